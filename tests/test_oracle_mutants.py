@@ -1,0 +1,133 @@
+"""Mutation check of the oracle's pins (CPU only).
+
+Each mutant is a copy of the oracle's C source with one plausible mistake
+planted (a dropped term, a wrong sign, index or operand order, a wrong
+constant, a wrong reading of the layout); it is compiled into a temporary
+directory and the pin battery runs against it in a child process.  Every
+mutant must fail at least one pin other than the golden digest, which is a
+regression check and not an independent pin (a mutant that crashes the
+child counts as caught).  The oracle itself is never
+modified.
+"""
+import os
+import subprocess
+import sys
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# (name, [(old, new), ...]); every `old` must occur exactly once in the source.
+MUTANTS = [
+    ("chunk drops its last square", [("for (int k = 1; k < 8; ++k)", "for (int k = 1; k < 7; ++k)")]),
+    ("tree drops its last level", [("for (int o = P / 2; o >= 1; o /= 2)", "for (int o = P / 2; o > 1; o /= 2)")]),
+    ("chunks of 4 instead of 8", [("int C = D / 8;", "int C = D / 4;"),
+                                  ("const float* xc = x + 8 * c;", "const float* xc = x + 4 * c;"),
+                                  ("for (int k = 1; k < 8; ++k)", "for (int k = 1; k < 4; ++k)")]),
+    ("mean over D-1", [("float ms = ss / (float)D;", "float ms = ss / (float)(D - 1);")]),
+    ("eps outside the root", [("float t = ms + eps;", "float t = ms;"),
+                              ("return 1.0f / rt;", "return 1.0f / (rt + eps);")]),
+    ("one rounding for 1/sqrt", [("return 1.0f / rt;", "return (float)(1.0 / sqrt((double)t));")]),
+    ("weight index", [("float y = xn * w[d];", "float y = xn * w[0];")]),
+    ("weight before the norm", [("float xn = x[d] * inv;\n        float y = xn * w[d];",
+                                 "float xn = x[d] * w[d];\n        float y = xn * inv;")]),
+    ("K normalised with the Q weight", [("const float* w = part == 0 ? wq : wk;",
+                                         "const float* w = part == 0 ? wq : wq;")]),
+    ("rotation sign", [("*u_out = h3o_round16(dtype, uc - vs);", "*u_out = h3o_round16(dtype, uc + vs);")]),
+    ("rotation operand", [("float us = u * s;", "float us = v * s;")]),
+    ("half-split pairs", [("h3o_rotate_pair(pb->in_dtype, cs[i], sn[i], n[2 * i], n[2 * i + 1],\n"
+                           "                                &dst[2 * i], &dst[2 * i + 1]);",
+                           "h3o_rotate_pair(pb->in_dtype, cs[i], sn[i], n[i], n[i + R / 2],\n"
+                           "                                &dst[i], &dst[i + R / 2]);")]),
+    ("every axis uses the t position", [("float p = (float)tok_pos[a];", "float p = (float)tok_pos[0];")]),
+    ("frequency exponent i/d", [("double expo = -(2.0 * (double)i) / (double)d;",
+                                 "double expo = -(1.0 * (double)i) / (double)d;")]),
+    ("pass-through channels zeroed", [("for (int d = R; d < D; ++d) dst[d] = n[d];",
+                                       "for (int d = R; d < D; ++d) dst[d] = 0;")]),
+    ("quadrant 1 cosine sign", [("case 1: s = cr; c = -sr; break;", "case 1: s = cr; c = sr; break;")]),
+    ("series coefficient", [("H3O_S5 = 0x1.111112p-7f", "H3O_S5 = 0x1.111110p-7f")]),
+    ("cosine series one term short", [("pc = fmaf(pc, r2, H3O_C4);", "")]),
+    ("V not the identity", [("for (int64_t e = 0; e < HD; ++e) yv[e] = vsrc[e];",
+                             "for (int64_t e = 0; e < HD; ++e) yv[e] = vsrc[e ^ 1];")]),
+    ("token-major output", [("return ((b * pb->heads + h) * pb->seq + s) * pb->head_dim;",
+                             "return ((b * pb->seq + s) * pb->heads + h) * pb->head_dim;")]),
+    ("valid prefix over the whole batch", [("return (r % pb->seq) < pb->valid_len;",
+                                            "return r < pb->valid_len;")]),
+    ("amax over padded rows", [("        if (!h3o_row_valid(pb, r)) continue;\n"
+                                "        h3o_row16_with(pb, qkv, wq, wk, pos, inv_freq, r, y[0], y[1], y[2]);\n"
+                                "        for (int t = 0; t < 3; ++t)\n"
+                                "            for (int64_t e = 0; e < HD; ++e) {",
+                                "        h3o_row16_with(pb, qkv, wq, wk, pos, inv_freq, r, y[0], y[1], y[2]);\n"
+                                "        for (int t = 0; t < 3; ++t)\n"
+                                "            for (int64_t e = 0; e < HD; ++e) {")]),
+    ("descale inverted", [("s = a / 448.0f;", "s = 448.0f / a;")]),
+    ("cast divides by the factor", [("float z = v * inv;", "float z = v / inv;")]),
+    ("static factor not inverted", [("i = 1.0f / tab;", "i = tab;")]),
+    ("e4m3 saturates late", [("if (a >= 448.0f) return (uint8_t)(sign | 0x7Eu);",
+                              "if (a > 480.0f) return (uint8_t)(sign | 0x7Eu);")]),
+    ("f16 rounds half up", [("uint32_t m = (uint32_t)rintf(n);", "uint32_t m = (uint32_t)floorf(n + 0.5f);")]),
+    ("bf16 subnormal exponent", [("h3o_round_sig(a, 7, -126, &E, &m);", "h3o_round_sig(a, 7, -125, &E, &m);")]),
+    ("f16 widening bias", [("else v = ldexpf((float)(man | 0x400), ex - 25);",
+                            "else v = ldexpf((float)(man | 0x400), ex - 24);")]),
+]
+
+_CHILD = r"""
+import os, sys
+sys.path[:0] = [{root!r}, os.path.join({root!r}, "tests")]
+os.environ["H3QK_PINS_QUICK"] = "1"
+import oracle_pins as P
+for p in P.PINS:
+    if p.__name__ == "pin_golden_digest":
+        continue
+    try:
+        p()
+    except Exception as e:
+        print("CAUGHT", p.__name__, type(e).__name__)
+        sys.exit(0)
+print("SURVIVED")
+"""
+
+
+def _make(src: str, edits, d: str) -> str:
+    for old, new in edits:
+        assert src.count(old) == 1, f"mutation target not unique or missing: {old[:60]!r}"
+        src = src.replace(old, new)
+    c = os.path.join(d, "m.c")
+    so = os.path.join(d, "m.so")
+    with open(c, "w") as f:
+        f.write(src)
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", so, c, "-lm"], check=True)
+    return so
+
+
+def _run(name_edits):
+    name, edits = name_edits
+    with open(oracle._SRC) as f:
+        src = f.read()
+    with tempfile.TemporaryDirectory() as d:
+        so = _make(src, edits, d)
+        env = dict(os.environ, H3QK_ORACLE_LIB=so)
+        r = subprocess.run([sys.executable, "-c", _CHILD.format(root=ROOT)], env=env,
+                           capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return name, f"CAUGHT (the mutant crashed, exit {r.returncode})"
+    return name, r.stdout.strip().splitlines()[-1] if r.stdout.strip() else "no output"
+
+
+def test_every_mutant_is_caught():
+    with ThreadPoolExecutor(max(1, min(8, os.cpu_count() or 1))) as ex:
+        results = list(ex.map(_run, MUTANTS))
+    survived = [(n, out) for n, out in results if not out.startswith("CAUGHT")]
+    assert not survived, survived
+
+
+@pytest.mark.parametrize("name,edits", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutation_targets_exist(name, edits):
+    with open(oracle._SRC) as f:
+        src = f.read()
+    for old, _ in edits:
+        assert src.count(old) == 1, (name, old[:60])
