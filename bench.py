@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused QK-prep path on one GB300 (or N independent
+replicas under torchrun).
+
+Workload: the untiled 544x960 latent grid, T32 x H34 x W60 = 65,280 tokens,
+24 heads x 128 channels, rotary 96 split 32/32/32 over (t, h, w), BF16 packed
+QKV ~N(0,1) with 0.1 % x50 outlier columns, seeded and synthetic.  One step
+prepares that tile twice, as the workload specifies: BF16 head-major Q/K/V,
+then e4m3 codes with dynamic per-tensor scales (amax pass + cast pass).
+
+Metric: algorithmic HBM bytes per second (16-bit: 12*H*D bytes per token;
+e4m3 dynamic: 15*H*D, the input read twice), with tokens/s and the fraction
+of the measured HBM copy peak beside it.  Inputs (1.2 GB) are larger than
+L2 (129 MB), so steps do not reuse each other's data in L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (test infrastructure, plain C) on
+the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from video_vae_decoder_qkv_gb300 import workloads as W  # noqa: E402
+
+METRIC = "fused QK-prep HBM GB/s and % of GB300 peak; tokens/s at 65k-token tile"
+SPEC16 = W.LATENT_65K
+SPEC8 = W.LATENT_65K_E4M3
+KERNEL_FILES = ["video_vae_decoder_qkv_gb300/csrc/h3qk_kernels.cuh",
+                "video_vae_decoder_qkv_gb300/csrc/h3qk_api.cu"]
+WORKLOAD = ("latent_65k: 544x960 latent grid T32xH34xW60 = 65,280 tokens, 24 heads x 128, "
+            "rotary 96 (32/32/32 over t,h,w), BF16 packed QKV ~N(0,1) with 0.1% x50 outlier "
+            "columns; each step: BF16 head-major out, then e4m3 out with dynamic scales")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling only: run the first N tokens of the tile (not a bench line)")
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------------------
+# ranks
+# --------------------------------------------------------------------------
+
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_max_sum(dist, elapsed_s: float, units: float, device=None):
+    """Max of the ranks' elapsed times and sum of their units (the whole-job
+    aggregate: value = units of all ranks / slowest rank's time)."""
+    if dist is None:
+        return elapsed_s, units
+    import torch
+
+    dev = device if device is not None else torch.device("cpu")
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "MEASURED_PEAKS.json hbm_gbs (measured copy)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_FILES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_sha256") != kernel_sha():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timings (baseline / reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_rows(inp, rows: int, threads: int) -> tuple[float, int]:
+    """Time the oracle on the first `rows` tokens of the workload, in both
+    output modes; returns (seconds, algorithmic bytes)."""
+    import oracle
+
+    def pb_of(spec):
+        return oracle.Problem(batch=1, seq=rows, heads=spec.heads, head_dim=spec.head_dim,
+                              rotary_dim=spec.rotary_dim, n_axes=spec.n_axes,
+                              axis_dims=tuple(spec.axis_dims), in_dtype=spec.in_dtype,
+                              out_kind=spec.out_kind, scale_mode=spec.scale_mode, eps=spec.eps,
+                              theta=spec.theta)
+
+    qkv, pos = inp.qkv[:rows], inp.pos[:rows]
+    t0 = time.perf_counter()
+    oracle.prepare(pb_of(SPEC16), qkv, inp.wq, inp.wk, pos, threads=threads)
+    oracle.prepare(pb_of(SPEC8), qkv, inp.wq, inp.wk, pos, threads=threads)
+    dt = time.perf_counter() - t0
+    hd = SPEC16.hd
+    return dt, rows * hd * (12 + 15)
+
+
+def cpu_threads() -> int:
+    return max(1, min(64, os.cpu_count() or 1))
+
+
+def run_reference(args):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return 0
+    import oracle
+
+    oracle.build()
+    inp = W.generate(SPEC16)
+    threads = cpu_threads()
+    # size each step so the whole run stays within a few minutes
+    cal_s, _ = oracle_rows(inp, 256, threads)
+    rate = 256 / max(cal_s, 1e-6)
+    budget = min(20.0, 150.0 / max(1, args.steps + args.warmup))
+    rows = int(max(64, min(SPEC16.rows, rate * budget)))
+    for _ in range(args.warmup):
+        oracle_rows(inp, rows, threads)
+    total_s, total_b = 0.0, 0
+    for _ in range(args.steps):
+        s, b = oracle_rows(inp, rows, threads)
+        total_s += s
+        total_b += b
+    gbs = total_b / total_s / 1e9
+    sample = f"first {rows} of 65,280 tokens per step, BF16 out then e4m3 dynamic"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded)",
+        "tokens_per_s": rows * args.steps / total_s,
+        "config": {"workload": WORKLOAD, "sample_tokens_per_step": rows},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
+# the CUDA path
+# --------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from video_vae_decoder_qkv_gb300 import h3qk, prepare
+
+    rank, world, local = rank_info()
+    if world != args.gpus and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    h3qk.lib()   # fail loudly now if the library is missing
+
+    spec16, spec8 = SPEC16, SPEC8
+    if args.tokens:
+        spec16 = SPEC16.with_(seq=args.tokens, grid=None)
+        spec8 = SPEC8.with_(seq=args.tokens, grid=None)
+    inp = W.generate(spec16)      # each rank: its own replica of the tile
+    N, H, D = spec16.rows, spec16.heads, spec16.head_dim
+    qkv_h = torch.from_numpy(inp.qkv.view(np.int16)).view(torch.bfloat16)
+    qkv = qkv_h.to(dev)
+    wq = torch.from_numpy(inp.wq).to(dev)
+    wk = torch.from_numpy(inp.wk).to(dev)
+    pos = torch.from_numpy(inp.pos).to(dev)
+    shape = (1, H, N, D)
+    out16 = tuple(torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    out8 = tuple(torch.empty(shape, dtype=torch.float8_e4m3fn, device=dev) for _ in range(3))
+    scales = torch.empty(3, dtype=torch.float32, device=dev)
+    ws = torch.zeros(4, dtype=torch.int32, device=dev)
+    common = dict(heads=H, head_dim=D, rotary_dim=spec16.rotary_dim, n_axes=3,
+                  axis_dims=spec16.axis_dims, theta=spec16.theta, eps=spec16.eps)
+    stream = torch.cuda.current_stream(dev)
+
+    def call16():
+        prepare(qkv, wq, wk, pos, out=out16, stream=stream, **common)
+
+    def call8():
+        prepare(qkv, wq, wk, pos, scale_mode="dynamic", out=out8, out_scales=scales, workspace=ws,
+                stream=stream, **common)
+
+    for _ in range(max(3, args.warmup)):
+        call16()
+        call8()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    h3qk.launch_count_reset()
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        call16()
+        ev[i][1].record(stream)
+        call8()
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    launches = h3qk.launch_count()
+    clocks = sampler.stop()
+    elapsed_s = start.elapsed_time(end) / 1e3
+    t16 = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    t8 = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev) / 1e3
+
+    bytes16 = spec16.algorithmic_bytes()
+    bytes8 = spec8.algorithmic_bytes()
+    step_bytes = bytes16 + bytes8
+    t_max, total_bytes = reduce_max_sum(dist, elapsed_s, step_bytes * K, dev)
+
+    # end to end through the public API with host buffers: the step's inputs
+    # copied from pinned host memory, both results copied back
+    E = max(1, min(args.e2e_steps, K))
+    qkv_pin = qkv_h.pin_memory()
+    wq_pin, wk_pin, pos_pin = (t.cpu().pin_memory() for t in (wq, wk, pos))
+    host16 = tuple(torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(3))
+    host8 = tuple(torch.empty(shape, dtype=torch.uint8).pin_memory() for _ in range(3))
+    host_sc = torch.empty(3, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (qkv_pin, wq_pin, wk_pin, pos_pin))
+    d2h = sum(t.numel() * t.element_size() for t in (*host16, *host8, host_sc))
+
+    def e2e_step():
+        qkv.copy_(qkv_pin, non_blocking=True)
+        wq.copy_(wq_pin, non_blocking=True)
+        wk.copy_(wk_pin, non_blocking=True)
+        pos.copy_(pos_pin, non_blocking=True)
+        call16()
+        call8()
+        for hdst, dsrc in zip(host16, out16):
+            hdst.copy_(dsrc, non_blocking=True)
+        for hdst, dsrc in zip(host8, out8):
+            hdst.copy_(dsrc.view(torch.uint8), non_blocking=True)
+        host_sc.copy_(scales, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(E):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = es.elapsed_time(ee) / 1e3
+    e2e_max, e2e_bytes = reduce_max_sum(dist, e2e_s, step_bytes * E, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.tokens:
+        rows = 16384
+        threads = cpu_threads()
+        s, b = oracle_rows(inp, rows, threads)
+        cpu = {"value": b / s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"first {rows} of 65,280 tokens, BF16 out then e4m3 dynamic, {threads} threads",
+               "seconds": s}
+
+    if rank == 0:
+        peak, peak_src = measured_peak()
+        value = total_bytes / t_max / 1e9
+        ach16 = bytes16 / t16 / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": 1e3 * t_max / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "io_dtype": "bf16 in; bf16 and e4m3 out",
+            "data": "synthetic (seeded numpy draws; random weights)",
+            "pct_of_peak": 100.0 * value / peak,
+            "tokens_per_s": N * K * world / t_max,
+            "config": {"workload": WORKLOAD if not args.tokens else
+                       f"profiling case: first {N} tokens of the 65k tile (not a bench line)",
+                       "tokens": N, "heads": H, "head_dim": D, "rotary_dim": spec16.rotary_dim, "global_batch": world,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (1.20 GB packed QKV per pass)"},
+            "kernels": {
+                "norm_rope_permute_bf16": {"ms": 1e3 * t16, "GB/s": ach16, "bytes": bytes16,
+                                           "tokens_per_s": N / t16},
+                "e4m3_dynamic_amax_plus_cast": {"ms": 1e3 * t8, "GB/s": bytes8 / t8 / 1e9,
+                                                "bytes": bytes8, "tokens_per_s": N / t8},
+            },
+            "roofline": {"bound": "hbm", "kernel": "qkprep_kernel<bf16, LPR=16, out16> (one launch)",
+                         "achieved": ach16, "peak": peak, "unit": "GB/s", "frac": ach16 / peak,
+                         "traffic": recorded_traffic(), "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": bytes16},
+            "e2e": {"value": e2e_bytes / e2e_max / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": E},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

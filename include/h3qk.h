@@ -1,0 +1,183 @@
+/*
+ * h3qk.h: C-ABI of libh3qk.so, the fused QK-prep path of the MiniMax-H3
+ * video VAE decoder and DiT attention on one GB300 (sm_103a).
+ *
+ * One call turns the packed QKV projection of a batch of token rows into
+ * head-major Q, K and V.  It applies a per-head RMS normalisation to Q and K,
+ * a partial multi-axis rotary embedding to Q and K, and optionally a
+ * per-tensor e4m3 cast (one amax pass and one cast pass with dynamic scales,
+ * or a cast with a static scale table).  Rows past a valid prefix are masked.
+ *
+ * Pages that define the operation:
+ *  - TensorRT-LLM pull request #21485, "cuDNN FP8 attention path for
+ *    MiniMax-H3 on SM107 under Ulysses": Summary bullet 2 (QK-norm, RoPE and
+ *    the FP8 per-tensor cast fused into one amax pass and one cast pass;
+ *    dynamic scales by default, a static scale table as an option), and the
+ *    commits that add the fused cast from the packed QKV projection, the
+ *    single-tensor norm_rope_tensor variant (identity for V), the per-item
+ *    valid length left out of the amax, and the custom-op aliasing fix
+ *    (an output never aliases an input).
+ *  - vllm-omni pull request #6607, MiniMax-H3 VAE decoder eager operators,
+ *    "Operations" table, row "Q/K normalization + RoPE": a fixed RMS
+ *    reduction order and explicit rounding points, bit-exact results.
+ *  - stable-diffusion.cpp pull request #19, "MiniMax-H3: sage takes the fused
+ *    RoPE op, faster video and audio VAE decode": q/k/v chunk-copied out of
+ *    the fused projection, the partial RoPE, the head-major
+ *    [head_dim, tokens, heads, batch] output and the fused per-head norm.
+ *
+ * Arithmetic (identical, bit for bit, to the CPU oracle of the test-suite):
+ *   per row r < tokens with (r mod S) < valid_len, head h, t in {Q, K}:
+ *     x[d]  = the 16-bit input widened to binary32;
+ *     ss    = sum of x[d]^2: chunks of 8 channels summed left to right, the
+ *             D/8 chunk sums (padded with zeros to a power of two) added by a
+ *             halving tree p[i] += p[i + o], o = P/2 ... 1;
+ *     inv   = 1 / sqrt(ss / D + eps), each operation correctly rounded;
+ *     n[d]  = round16((x[d] * inv) * w_t[d]);
+ *     pairs (2i, 2i+1) of the first rotary_dim channels, cut into n_axes
+ *     segments of widths axis_dims[a], rotate by
+ *       ang = pos[r][a] * theta^(-2i'/axis_dims[a]), i' the pair index
+ *             within its segment (inverse frequency rounded to binary32
+ *             once on the host),
+ *       (u, v) -> (round16(u cos - v sin), round16(u sin + v cos)),
+ *     with sin/cos from the library's own Cody-Waite + Taylor routine;
+ *     channels >= rotary_dim pass through; V is copied unchanged.
+ *   e4m3: amax_t = max |y| over the 16-bit results of the valid rows;
+ *     dynamic: scale_t = amax_t / 448, factor = 448 / amax_t; static:
+ *     scale_t = table[t], factor = 1 / table[t]; a zero, subnormal,
+ *     infinite or NaN amax or table entry gives scale = factor = 1;
+ *     code = e4m3 round-to-nearest-even, saturating at +-448, of y * factor.
+ */
+#ifndef H3QK_H
+#define H3QK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream).  NULL is the legacy default
+ * stream of the calling thread's current device. */
+typedef struct CUstream_st* h3qk_stream_t;
+
+typedef enum h3qk_status {
+    H3QK_OK = 0,
+    H3QK_ERR_INVALID_ARG = 1, /* a null pointer, a size or option out of range */
+    H3QK_ERR_MISALIGNED = 2,  /* a pointer or row stride breaks the alignment rules */
+    H3QK_ERR_ALIAS = 3,       /* an output overlaps an input or another output */
+    H3QK_ERR_CUDA = 4         /* the CUDA runtime refused a launch; see h3qk_last_cuda_error */
+} h3qk_status;
+
+typedef enum h3qk_dtype {
+    H3QK_DTYPE_DEFAULT = 0, /* in h3qk_opts.in_dtype only: see there */
+    H3QK_FP16 = 1,          /* IEEE binary16 */
+    H3QK_BF16 = 2,          /* bfloat16 */
+    H3QK_E4M3 = 3           /* OCP 8-bit E4M3FN codes (output only) */
+} h3qk_dtype;
+
+typedef enum h3qk_scale_mode {
+    H3QK_SCALE_NONE = 0,    /* 16-bit output, no cast */
+    H3QK_SCALE_DYNAMIC = 1, /* amax pass, then cast with amax / 448 */
+    H3QK_SCALE_STATIC = 2   /* cast with the caller's descale table */
+} h3qk_scale_mode;
+
+/* Optional arguments.  Pass NULL for all defaults, or fill one with
+ * h3qk_opts_init() and change fields.  Enum-valued fields are int32_t. */
+typedef struct h3qk_opts {
+    int32_t in_dtype;        /* h3qk_dtype of qkv: H3QK_FP16 or H3QK_BF16.
+                                DEFAULT: out_dtype when that is 16-bit, else BF16 */
+    int32_t n_axes;          /* 3: (t, h, w) positions; 1: 1-D positions.  Default 3 */
+    int32_t axis_dims[3];    /* widths of the rotary segments, even, summing to
+                                rotary_dim.  All zero (default): rotary_dim/3 each
+                                (n_axes 3) or rotary_dim (n_axes 1) */
+    float eps;               /* RMSNorm epsilon, default 1e-6 */
+    int64_t batch;           /* B >= 1: tokens = B * S rows, S rows per item.
+                                valid_len applies to every item.  Default 1 */
+    int64_t qkv_row_stride;  /* elements between consecutive packed rows; a
+                                multiple of 8, >= 3*heads*head_dim.  0 (default):
+                                3*heads*head_dim */
+    double theta;            /* rotary base, default 10000 */
+    const float* static_scales; /* device float[3], descales (q, k, v); required
+                                   when scale_mode is STATIC, read by the kernel */
+    void* workspace;         /* device memory of >= h3qk_workspace_bytes() bytes,
+                                16-byte aligned, required when scale_mode is
+                                DYNAMIC; holds the amax words of one call, so
+                                calls that may overlap need their own */
+    size_t workspace_bytes;  /* size of workspace */
+} h3qk_opts;
+
+/* Fill *opts with the defaults listed above. */
+void h3qk_opts_init(h3qk_opts* opts);
+
+/* Bytes of device workspace a DYNAMIC call needs (16). */
+size_t h3qk_workspace_bytes(void);
+
+/*
+ * h3qk_prepare: the whole path for one batch of packed QKV rows.
+ *
+ * Arguments (every pointer is device memory owned by the caller; the library
+ * allocates nothing and keeps no pointer after the call returns):
+ *   qkv        16-bit [tokens, row_stride] row-major, row r = [Q | K | V],
+ *              each heads*head_dim values with head h's channels at
+ *              h*head_dim; 16-byte aligned.  Read only.
+ *   norm_wq    float[head_dim], RMSNorm weight of Q, shared by the heads;
+ *              16-byte aligned.  Read only.
+ *   norm_wk    float[head_dim], RMSNorm weight of K; 16-byte aligned.
+ *   positions  int32 [tokens, n_axes] row-major: each row's position on each
+ *              axis (tile-local grid indices, or 0..S-1 for 1-D).  May be
+ *              NULL when rotary_dim is 0.  Read only.
+ *   tokens     B*S >= 0 rows.  0 is a valid empty call: qkv, positions and
+ *              the three row outputs may then be NULL; in e4m3 modes the
+ *              descales are still written (1 for DYNAMIC, the table for
+ *              STATIC).
+ *   heads      H >= 1.
+ *   head_dim   D: a multiple of 8 in [8, 256].
+ *   rotary_dim R: even, 0 <= R <= D.
+ *   valid_len  0 <= valid_len <= S: rows s >= valid_len of every item are
+ *              neither read for the amax nor written.
+ *   out_dtype  H3QK_FP16 / H3QK_BF16 (must equal the input type) with
+ *              scale_mode NONE, or H3QK_E4M3 with DYNAMIC or STATIC.
+ *   out_q, out_k, out_v  [B, H, S, D] contiguous, 2 bytes (16-bit) or 1 byte
+ *              (e4m3) per element; 16-byte aligned; pairwise disjoint and
+ *              disjoint from every input.  Rows past valid_len keep their
+ *              previous bytes.
+ *   out_scales float[3] descales (q, k, v) written in e4m3 modes (NULL
+ *              allowed with scale_mode NONE); never the static table itself.
+ *   opts       NULL or see h3qk_opts.
+ *   stream     the stream the kernels are enqueued on.
+ *
+ * Errors: every argument is checked on the host before anything is
+ * enqueued; a check that fails returns its status and enqueues nothing.
+ * H3QK_ERR_CUDA reports a failed launch (h3qk_last_cuda_error() gives the
+ * CUDA error code of the calling thread's last failure).  The call is
+ * asynchronous on `stream`: it never synchronises, never aborts and never
+ * traps; results are ready when the stream reaches them.
+ */
+h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* norm_wk,
+                         const int32_t* positions, int64_t tokens, int32_t heads,
+                         int32_t head_dim, int32_t rotary_dim, int64_t valid_len,
+                         h3qk_dtype out_dtype, h3qk_scale_mode scale_mode, void* out_q,
+                         void* out_k, void* out_v, float* out_scales, const h3qk_opts* opts,
+                         h3qk_stream_t stream);
+
+/* A static, human-readable name of a status. */
+const char* h3qk_status_string(h3qk_status status);
+
+/* The cudaError_t code of the calling thread's last H3QK_ERR_CUDA (0 if none). */
+int h3qk_last_cuda_error(void);
+
+/* Number of kernel launches the calling thread's h3qk calls have enqueued
+ * since the last reset (a "this path ran" counter); reset with
+ * h3qk_launch_count_reset(). */
+uint64_t h3qk_launch_count(void);
+void h3qk_launch_count_reset(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int h3qk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H3QK_H */

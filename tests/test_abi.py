@@ -1,0 +1,119 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/h3qk.h declares, lays out h3qk_opts as the binding does, and rejects
+bad arguments on the host before touching CUDA.  The fake addresses below
+are never dereferenced: every call here fails a host-side check first."""
+import ctypes
+
+import pytest
+
+from video_vae_decoder_qkv_gb300 import h3qk
+
+H, D, R = 4, 64, 48
+N = 48
+A = 0x10000000          # fake, 256-byte aligned device addresses
+QKV, WQ, WK, POS = A, A + 0x1000000, A + 0x1001000, A + 0x1002000
+OQ, OK_, OV, SC, TAB, WS = (A + 0x2000000, A + 0x3000000, A + 0x4000000, A + 0x5000000,
+                            A + 0x5001000, A + 0x5002000)
+
+
+@pytest.fixture(scope="module")
+def L():
+    return h3qk.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = h3qk.declared_functions()
+    assert "h3qk_prepare" in names and len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_opts_layout_and_defaults(L):
+    o = h3qk.default_opts()
+    assert ctypes.sizeof(h3qk.Opts) == 72
+    assert o.in_dtype == 0 and o.n_axes == 3 and list(o.axis_dims) == [0, 0, 0]
+    assert o.eps == pytest.approx(1e-6, rel=1e-7) and o.batch == 1 and o.qkv_row_stride == 0
+    assert o.theta == 10000.0 and not o.static_scales and not o.workspace and o.workspace_bytes == 0
+    assert L.h3qk_workspace_bytes() == 16
+    assert L.h3qk_version() >= 100
+
+
+def test_status_strings(L):
+    for s in range(5):
+        assert h3qk.status_string(s)
+    assert h3qk.status_string(99) == "unknown status"
+
+
+def call(**kw):
+    a = dict(qkv=QKV, norm_wq=WQ, norm_wk=WK, positions=POS, tokens=N, heads=H, head_dim=D,
+             rotary_dim=R, valid_len=N, out_dtype=h3qk.BF16, scale_mode=h3qk.SCALE_NONE,
+             out_q=OQ, out_k=OK_, out_v=OV, out_scales=None, opts=None, stream=None)
+    a.update(kw)
+    return h3qk.prepare_ptr(**a)
+
+
+def opts(**kw):
+    o = h3qk.default_opts()
+    for k, v in kw.items():
+        if k == "axis_dims":
+            o.axis_dims = (ctypes.c_int32 * 3)(*v)
+        else:
+            setattr(o, k, v)
+    return o
+
+
+@pytest.mark.parametrize("kw", [
+    dict(qkv=None), dict(norm_wq=None), dict(norm_wk=None), dict(positions=None), dict(out_q=None),
+    dict(out_v=None), dict(tokens=-1), dict(heads=0), dict(head_dim=12), dict(head_dim=264),
+    dict(head_dim=0), dict(rotary_dim=47), dict(rotary_dim=66), dict(rotary_dim=-2),
+    dict(valid_len=N + 1), dict(valid_len=-1), dict(out_dtype=7),
+    dict(out_dtype=h3qk.FP16, opts=opts(in_dtype=h3qk.BF16)),
+    dict(scale_mode=h3qk.SCALE_DYNAMIC), dict(out_dtype=h3qk.E4M3),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_STATIC, out_scales=SC),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_STATIC, out_scales=None, opts=opts(static_scales=TAB)),
+    dict(opts=opts(batch=5)), dict(opts=opts(batch=0)), dict(opts=opts(n_axes=2)),
+    dict(opts=opts(axis_dims=(16, 16, 14))), dict(opts=opts(axis_dims=(15, 17, 16))),
+    dict(opts=opts(n_axes=1, axis_dims=(24, 24, 0))), dict(rotary_dim=46),
+    dict(opts=opts(eps=-1.0)), dict(opts=opts(theta=0.0)), dict(opts=opts(in_dtype=3)),
+    dict(opts=opts(qkv_row_stride=3 * H * D - 8)),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC,
+         opts=opts(workspace=WS, workspace_bytes=8)),
+])
+def test_invalid_arguments(kw):
+    assert call(**kw) == h3qk.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [
+    dict(qkv=QKV + 8), dict(out_k=OK_ + 2), dict(norm_wq=WQ + 4), dict(positions=POS + 2),
+    dict(opts=opts(qkv_row_stride=3 * H * D + 4)),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC + 2,
+         opts=opts(workspace=WS, workspace_bytes=16)),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC,
+         opts=opts(workspace=WS + 4, workspace_bytes=16)),
+])
+def test_misaligned(kw):
+    assert call(**kw) == h3qk.ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("kw", [
+    dict(out_k=OQ), dict(out_v=OQ + 256), dict(out_q=QKV), dict(out_q=QKV + 4096),
+    dict(out_v=WK), dict(out_q=POS),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_STATIC, out_scales=TAB, opts=opts(static_scales=TAB)),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC,
+         opts=opts(workspace=OQ + 16, workspace_bytes=16)),
+])
+def test_aliasing_outputs(kw):
+    assert call(**kw) == h3qk.ERR_ALIAS
+
+
+def test_valid_call_without_a_device_reports_cuda_error():
+    """On a host with no usable GPU a valid call gets as far as the launch and
+    reports H3QK_ERR_CUDA (a launch on a real GPU would use these fake
+    addresses, so the call is made only where no device exists)."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; the fake addresses must not reach a launch")
+    assert call() == h3qk.ERR_CUDA
+    assert h3qk.lib().h3qk_last_cuda_error() != 0

@@ -1,0 +1,11 @@
+"""GB300-native fused QK-prep for the MiniMax-H3 video VAE decoder and DiT
+attention: per-head RMSNorm of Q and K, partial multi-axis RoPE, the permute
+of the packed QKV projection to head-major Q/K/V, and an optional per-tensor
+e4m3 cast (dynamic or static scales, valid-prefix mask).
+
+The path is libh3qk.so (hand-written sm_103a CUDA behind the C-ABI in
+include/h3qk.h); ``prepare`` is its thin Python binding.
+"""
+from .h3qk import H3QKError, prepare  # noqa: F401
+
+__all__ = ["prepare", "H3QKError"]

@@ -1,0 +1,293 @@
+// Host side of libh3qk: argument checks, rotary tables and kernel launches
+// behind the C-ABI declared in include/h3qk.h.
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "h3qk.h"
+#include "h3qk_kernels.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+thread_local uint64_t g_launches = 0;
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
+    if (dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    if (dev < kMaxDevices) g_sm_count[dev] = n;
+    return n;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range range_of(const void* p, int64_t bytes)
+{
+    uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + static_cast<uintptr_t>(bytes > 0 ? bytes : 0)};
+}
+
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+int next_pow2(int v)
+{
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+template <bool BF16, int LPR>
+cudaError_t launch_mode(int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
+{
+    switch (mode) {
+    case h3qk::kOut16:
+        h3qk::qkprep_kernel<BF16, LPR, h3qk::kOut16><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        break;
+    case h3qk::kAmax:
+        h3qk::qkprep_kernel<BF16, LPR, h3qk::kAmax><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        break;
+    default:
+        h3qk::qkprep_kernel<BF16, LPR, h3qk::kCast><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        break;
+    }
+    ++g_launches;
+    return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t launch_lpr(int lpr, int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
+{
+    switch (lpr) {
+    case 1: return launch_mode<BF16, 1>(mode, p, blocks, st);
+    case 2: return launch_mode<BF16, 2>(mode, p, blocks, st);
+    case 4: return launch_mode<BF16, 4>(mode, p, blocks, st);
+    case 8: return launch_mode<BF16, 8>(mode, p, blocks, st);
+    case 16: return launch_mode<BF16, 16>(mode, p, blocks, st);
+    default: return launch_mode<BF16, 32>(mode, p, blocks, st);
+    }
+}
+
+cudaError_t launch(bool bf16, int lpr, int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
+{
+    return bf16 ? launch_lpr<true>(lpr, mode, p, blocks, st) : launch_lpr<false>(lpr, mode, p, blocks, st);
+}
+
+h3qk_status fail_cuda(cudaError_t e)
+{
+    g_last_cuda_error = static_cast<int>(e);
+    return H3QK_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+void h3qk_opts_init(h3qk_opts* o)
+{
+    if (!o) return;
+    std::memset(o, 0, sizeof(*o));
+    o->in_dtype = H3QK_DTYPE_DEFAULT;
+    o->n_axes = 3;
+    o->eps = 1e-6f;
+    o->batch = 1;
+    o->qkv_row_stride = 0;
+    o->theta = 10000.0;
+}
+
+size_t h3qk_workspace_bytes(void) { return 16; }
+
+const char* h3qk_status_string(h3qk_status s)
+{
+    switch (s) {
+    case H3QK_OK: return "ok";
+    case H3QK_ERR_INVALID_ARG: return "invalid argument";
+    case H3QK_ERR_MISALIGNED: return "misaligned pointer or row stride";
+    case H3QK_ERR_ALIAS: return "an output overlaps an input or another output";
+    case H3QK_ERR_CUDA: return "CUDA launch failed";
+    }
+    return "unknown status";
+}
+
+int h3qk_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint64_t h3qk_launch_count(void) { return g_launches; }
+
+void h3qk_launch_count_reset(void) { g_launches = 0; }
+
+int h3qk_version(void) { return 100; }
+
+h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* norm_wk,
+                         const int32_t* positions, int64_t tokens, int32_t heads,
+                         int32_t head_dim, int32_t rotary_dim, int64_t valid_len,
+                         h3qk_dtype out_dtype, h3qk_scale_mode scale_mode, void* out_q,
+                         void* out_k, void* out_v, float* out_scales, const h3qk_opts* opts,
+                         h3qk_stream_t stream)
+{
+    h3qk_opts o;
+    h3qk_opts_init(&o);
+    if (opts) o = *opts;
+
+    // ---- sizes and options -------------------------------------------------
+    if (tokens < 0 || heads < 1 || heads > 65536) return H3QK_ERR_INVALID_ARG;
+    if (head_dim < 8 || head_dim > 256 || head_dim % 8) return H3QK_ERR_INVALID_ARG;
+    if (rotary_dim < 0 || rotary_dim > head_dim || rotary_dim % 2) return H3QK_ERR_INVALID_ARG;
+    if (o.batch < 1 || tokens % o.batch) return H3QK_ERR_INVALID_ARG;
+    const int64_t S = tokens / o.batch;
+    if (valid_len < 0 || valid_len > S) return H3QK_ERR_INVALID_ARG;
+    if (o.n_axes != 1 && o.n_axes != 3) return H3QK_ERR_INVALID_ARG;
+    int dims[3] = {o.axis_dims[0], o.axis_dims[1], o.axis_dims[2]};
+    if (dims[0] == 0 && dims[1] == 0 && dims[2] == 0) {
+        if (o.n_axes == 3) {
+            if (rotary_dim % 3) return H3QK_ERR_INVALID_ARG;
+            dims[0] = dims[1] = dims[2] = rotary_dim / 3;
+        } else {
+            dims[0] = rotary_dim;
+        }
+    }
+    int dim_sum = 0;
+    for (int a = 0; a < 3; ++a) {
+        if (a >= o.n_axes && dims[a] != 0) return H3QK_ERR_INVALID_ARG;
+        if (dims[a] < 0 || dims[a] % 2) return H3QK_ERR_INVALID_ARG;
+        dim_sum += dims[a];
+    }
+    if (dim_sum != rotary_dim) return H3QK_ERR_INVALID_ARG;
+    if (!(o.eps >= 0.0f) || !std::isfinite(o.eps)) return H3QK_ERR_INVALID_ARG;
+    if (!(o.theta > 0.0) || !std::isfinite(o.theta)) return H3QK_ERR_INVALID_ARG;
+
+    int in_dtype = o.in_dtype;
+    if (in_dtype == H3QK_DTYPE_DEFAULT) in_dtype = (out_dtype == H3QK_FP16) ? H3QK_FP16 : H3QK_BF16;
+    if (in_dtype != H3QK_FP16 && in_dtype != H3QK_BF16) return H3QK_ERR_INVALID_ARG;
+    const bool e4m3 = out_dtype == H3QK_E4M3;
+    if (out_dtype == H3QK_FP16 || out_dtype == H3QK_BF16) {
+        if (out_dtype != in_dtype || scale_mode != H3QK_SCALE_NONE) return H3QK_ERR_INVALID_ARG;
+    } else if (e4m3) {
+        if (scale_mode != H3QK_SCALE_DYNAMIC && scale_mode != H3QK_SCALE_STATIC) return H3QK_ERR_INVALID_ARG;
+    } else {
+        return H3QK_ERR_INVALID_ARG;
+    }
+
+    const int64_t HD = static_cast<int64_t>(heads) * head_dim;
+    const int64_t stride = o.qkv_row_stride ? o.qkv_row_stride : 3 * HD;
+    if (stride < 3 * HD) return H3QK_ERR_INVALID_ARG;
+    // Byte sizes must stay far from int64 overflow.
+    if (tokens > 0 && (stride > (INT64_C(1) << 40) / tokens || HD > (INT64_C(1) << 40) / tokens))
+        return H3QK_ERR_INVALID_ARG;
+
+    // ---- pointers ----------------------------------------------------------
+    // An empty call (tokens == 0) reads and writes no row, so its row buffers
+    // may be NULL (an empty torch tensor has a null data pointer).
+    if (!norm_wq || !norm_wk) return H3QK_ERR_INVALID_ARG;
+    if (tokens > 0 && (!qkv || !out_q || !out_k || !out_v)) return H3QK_ERR_INVALID_ARG;
+    if (tokens > 0 && rotary_dim > 0 && !positions) return H3QK_ERR_INVALID_ARG;
+    if (e4m3 && !out_scales) return H3QK_ERR_INVALID_ARG;
+    if (e4m3 && scale_mode == H3QK_SCALE_STATIC && !o.static_scales) return H3QK_ERR_INVALID_ARG;
+    if (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC &&
+        (!o.workspace || o.workspace_bytes < h3qk_workspace_bytes()))
+        return H3QK_ERR_INVALID_ARG;
+
+    if (stride % 8) return H3QK_ERR_MISALIGNED;
+    if (!aligned(qkv, 16) || !aligned(norm_wq, 16) || !aligned(norm_wk, 16)) return H3QK_ERR_MISALIGNED;
+    if (!aligned(out_q, 16) || !aligned(out_k, 16) || !aligned(out_v, 16)) return H3QK_ERR_MISALIGNED;
+    if (positions && !aligned(positions, 4)) return H3QK_ERR_MISALIGNED;
+    if (e4m3 && !aligned(out_scales, 4)) return H3QK_ERR_MISALIGNED;
+    if (e4m3 && scale_mode == H3QK_SCALE_STATIC && !aligned(o.static_scales, 4)) return H3QK_ERR_MISALIGNED;
+    if (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC && !aligned(o.workspace, 16)) return H3QK_ERR_MISALIGNED;
+
+    // ---- aliasing: outputs never overlap inputs or each other ---------------
+    const int64_t esz = e4m3 ? 1 : 2;
+    const Range outs[4] = {range_of(out_q, tokens * HD * esz), range_of(out_k, tokens * HD * esz),
+                           range_of(out_v, tokens * HD * esz),
+                           range_of(out_scales, e4m3 ? 12 : 0)};
+    const Range ins[6] = {
+        range_of(qkv, tokens > 0 ? ((tokens - 1) * stride + 3 * HD) * 2 : 0),
+        range_of(norm_wq, head_dim * 4), range_of(norm_wk, head_dim * 4),
+        range_of(positions, positions ? tokens * o.n_axes * 4 : 0),
+        range_of(o.static_scales, (e4m3 && scale_mode == H3QK_SCALE_STATIC) ? 12 : 0),
+        range_of(o.workspace, (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC) ? 16 : 0)};
+    for (int i = 0; i < 4; ++i) {
+        for (int k = i + 1; k < 4; ++k)
+            if (overlap(outs[i], outs[k])) return H3QK_ERR_ALIAS;
+        for (int k = 0; k < 6; ++k)
+            if (overlap(outs[i], ins[k])) return H3QK_ERR_ALIAS;
+    }
+
+    // ---- launch parameters ---------------------------------------------------
+    h3qk::Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.qkv = static_cast<const uint16_t*>(qkv);
+    p.wq = norm_wq;
+    p.wk = norm_wk;
+    p.pos = positions;
+    p.out[0] = out_q;
+    p.out[1] = out_k;
+    p.out[2] = out_v;
+    p.out_scales = out_scales;
+    p.amax_words = static_cast<unsigned int*>(o.workspace);
+    p.scale_words = scale_mode == H3QK_SCALE_DYNAMIC
+                        ? p.amax_words
+                        : reinterpret_cast<const unsigned int*>(o.static_scales);
+    p.rows = tokens;
+    p.seq = S;
+    p.valid_len = valid_len;
+    p.row_stride = stride;
+    p.heads = heads;
+    p.head_dim = head_dim;
+    p.rotary_dim = rotary_dim;
+    p.n_axes = o.n_axes;
+    p.chunks = head_dim / 8;
+    p.dynamic = scale_mode == H3QK_SCALE_DYNAMIC ? 1 : 0;
+    p.eps = o.eps;
+    p.inv_d = (head_dim & (head_dim - 1)) == 0 ? 1.0f / static_cast<float>(head_dim) : 0.0f;
+    // Rotary inverse frequencies theta^(-2i/d_a), in double, rounded once.
+    int pair = 0;
+    for (int a = 0; a < o.n_axes; ++a)
+        for (int i = 0; i < dims[a] / 2; ++i, ++pair) {
+            const double expo = -(2.0 * static_cast<double>(i)) / static_cast<double>(dims[a]);
+            p.inv_freq[pair] = static_cast<float>(std::pow(o.theta, expo));
+            p.axis[pair] = static_cast<uint8_t>(a);
+        }
+
+    const int lpr = next_pow2(head_dim / 8);
+    const int64_t tpw = 32 / lpr;
+    const int64_t groups = (tokens + tpw - 1) / tpw;
+    const int64_t want = (groups + h3qk::kWarpsPerBlock - 1) / h3qk::kWarpsPerBlock;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+    const int blocks = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const bool bf16 = in_dtype == H3QK_BF16;
+    cudaError_t e;
+
+    if (!e4m3) {
+        if (tokens == 0 || valid_len == 0) return H3QK_OK;
+        e = launch(bf16, lpr, h3qk::kOut16, p, blocks, st);
+        return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
+    }
+    if (scale_mode == H3QK_SCALE_DYNAMIC) {
+        h3qk::amax_init_kernel<<<1, 32, 0, st>>>(p.amax_words);
+        ++g_launches;
+        if ((e = cudaGetLastError()) != cudaSuccess) return fail_cuda(e);
+        if (tokens > 0 && valid_len > 0) {
+            e = launch(bf16, lpr, h3qk::kAmax, p, blocks, st);
+            if (e != cudaSuccess) return fail_cuda(e);
+        }
+    }
+    e = launch(bf16, lpr, h3qk::kCast, p, blocks, st);
+    return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
+}
+
+}  // extern "C"

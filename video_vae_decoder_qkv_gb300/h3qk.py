@@ -1,0 +1,186 @@
+"""Python binding of libh3qk.so (ctypes).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  When the
+library has not been built this module raises instead of computing anything
+another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libh3qk.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "h3qk.h")
+
+DTYPE_DEFAULT, FP16, BF16, E4M3 = 0, 1, 2, 3
+SCALE_NONE, SCALE_DYNAMIC, SCALE_STATIC = 0, 1, 2
+OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_ALIAS, ERR_CUDA = 0, 1, 2, 3, 4
+_SCALE_NAMES = {"none": SCALE_NONE, "dynamic": SCALE_DYNAMIC, "static": SCALE_STATIC}
+
+
+class H3QKError(RuntimeError):
+    def __init__(self, status: int, name: str, cuda_error: int = 0):
+        msg = f"h3qk_prepare failed: {name} (status {status})"
+        if status == ERR_CUDA:
+            msg += f", cudaError {cuda_error}"
+        super().__init__(msg)
+        self.status = status
+        self.cuda_error = cuda_error
+
+
+class Opts(ctypes.Structure):
+    """Mirror of h3qk_opts (include/h3qk.h)."""
+
+    _fields_ = [
+        ("in_dtype", ctypes.c_int32),
+        ("n_axes", ctypes.c_int32),
+        ("axis_dims", ctypes.c_int32 * 3),
+        ("eps", ctypes.c_float),
+        ("batch", ctypes.c_int64),
+        ("qkv_row_stride", ctypes.c_int64),
+        ("theta", ctypes.c_double),
+        ("static_scales", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libh3qk.so; raise if it was not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m video_vae_decoder_qkv_gb300.build` "
+                "(or __graft_entry__.build()); there is no other implementation of this path")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.h3qk_prepare.restype = ctypes.c_int
+        L.h3qk_prepare.argtypes = [P, P, P, P, I64, I32, I32, I32, I64, ctypes.c_int, ctypes.c_int,
+                                   P, P, P, P, ctypes.POINTER(Opts), P]
+        L.h3qk_opts_init.restype = None
+        L.h3qk_opts_init.argtypes = [ctypes.POINTER(Opts)]
+        L.h3qk_workspace_bytes.restype = ctypes.c_size_t
+        L.h3qk_status_string.restype = ctypes.c_char_p
+        L.h3qk_status_string.argtypes = [ctypes.c_int]
+        L.h3qk_last_cuda_error.restype = ctypes.c_int
+        L.h3qk_launch_count.restype = ctypes.c_uint64
+        L.h3qk_launch_count_reset.restype = None
+        L.h3qk_version.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/h3qk.h declares."""
+    with open(HEADER) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(h3qk_[a-z0-9_]+)\s*\(", src)))
+
+
+def default_opts() -> Opts:
+    o = Opts()
+    lib().h3qk_opts_init(ctypes.byref(o))
+    return o
+
+
+def status_string(status: int) -> str:
+    return lib().h3qk_status_string(status).decode()
+
+
+def launch_count() -> int:
+    return int(lib().h3qk_launch_count())
+
+
+def launch_count_reset() -> None:
+    lib().h3qk_launch_count_reset()
+
+
+def prepare_ptr(qkv, norm_wq, norm_wk, positions, tokens, heads, head_dim, rotary_dim, valid_len,
+                out_dtype, scale_mode, out_q, out_k, out_v, out_scales, opts: Opts | None, stream) -> int:
+    """Call h3qk_prepare with raw integer addresses; returns the status."""
+    L = lib()
+    return int(L.h3qk_prepare(qkv, norm_wq, norm_wk, positions, int(tokens), int(heads),
+                              int(head_dim), int(rotary_dim), int(valid_len), int(out_dtype),
+                              int(scale_mode), out_q, out_k, out_v, out_scales,
+                              ctypes.byref(opts) if opts is not None else None, stream))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def prepare(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rotary_dim: int,
+            batch: int = 1, valid_len: int | None = None, scale_mode: str = "none",
+            n_axes: int | None = None, axis_dims=None, theta: float = 10000.0, eps: float = 1e-6,
+            static_scales=None, out=None, out_scales=None, workspace=None, stream=None):
+    """The fused QK-prep path on torch CUDA tensors.
+
+    qkv: fp16/bf16 [tokens, row_stride] (row stride a multiple of 8 elements,
+    >= 3*heads*head_dim); norm_wq / norm_wk: float32 [head_dim]; positions:
+    int32 [tokens, n_axes].  scale_mode: "none" (16-bit out, the input type),
+    "dynamic" or "static" (e4m3 out; static needs ``static_scales``, a
+    float32 [3] CUDA tensor of descales).  Returns (q, k, v, scales): q, k, v
+    head-major [batch, heads, S, head_dim], scales a float32 [3] tensor of
+    descales in e4m3 modes, else None.  ``out``, ``out_scales`` and
+    ``workspace`` reuse caller buffers (rows past valid_len of ``out`` keep
+    their contents).
+    """
+    import torch
+
+    if qkv.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("qkv must be float16 or bfloat16")
+    if qkv.dim() != 2 or qkv.stride(1) != 1:
+        raise ValueError("qkv must be 2-D [tokens, row_stride] with unit inner stride")
+    tokens = qkv.shape[0]
+    if tokens % batch:
+        raise ValueError("tokens must be a multiple of batch")
+    seq = tokens // batch
+    if valid_len is None:
+        valid_len = seq
+    mode = _SCALE_NAMES[scale_mode]
+    in_dt = FP16 if qkv.dtype == torch.float16 else BF16
+    out_dt = in_dt if mode == SCALE_NONE else E4M3
+    if n_axes is None:
+        n_axes = positions.shape[1] if positions is not None and positions.dim() == 2 else 3
+    dev = qkv.device
+    shape = (batch, heads, seq, head_dim)
+    if out is None:
+        tdt = qkv.dtype if out_dt != E4M3 else torch.float8_e4m3fn
+        out = tuple(torch.empty(shape, dtype=tdt, device=dev) for _ in range(3))
+    q, k, v = out
+    if out_dt == E4M3 and out_scales is None:
+        out_scales = torch.empty(3, dtype=torch.float32, device=dev)
+    if mode == SCALE_DYNAMIC and workspace is None:
+        workspace = torch.empty(int(lib().h3qk_workspace_bytes()) // 4, dtype=torch.int32, device=dev)
+    o = default_opts()
+    o.in_dtype = in_dt
+    o.n_axes = n_axes
+    if axis_dims is not None:
+        dims = list(axis_dims) + [0] * (3 - len(axis_dims))
+        o.axis_dims = (ctypes.c_int32 * 3)(*dims)
+    o.eps = eps
+    o.batch = batch
+    o.qkv_row_stride = qkv.stride(0)
+    o.theta = theta
+    o.static_scales = _ptr(static_scales)
+    if workspace is not None:
+        o.workspace = workspace.data_ptr()
+        o.workspace_bytes = workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    st = prepare_ptr(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens,
+                     heads, head_dim, rotary_dim, valid_len, out_dt, mode, q.data_ptr(),
+                     k.data_ptr(), v.data_ptr(), _ptr(out_scales) if out_dt == E4M3 else None, o, stream)
+    if st != OK:
+        raise H3QKError(st, status_string(st), int(lib().h3qk_last_cuda_error()))
+    return q, k, v, (out_scales if out_dt == E4M3 else None)

@@ -28,6 +28,8 @@ token n = (t*Hg + h)*Wg + w, or 0..S-1 for 1-D positions.
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -155,10 +157,19 @@ def generate(spec: Spec) -> Inputs:
     static = head.uniform(0.01, 0.1, 3).astype(np.float32)
 
     qkv = np.zeros((spec.rows, spec.row_stride), np.uint16)
-    for c0 in range(0, spec.rows, _CHUNK_ROWS):
+
+    def fill(c0: int) -> None:
+        # each chunk has its own seed, so chunks may be drawn in any order
         c1 = min(spec.rows, c0 + _CHUNK_ROWS)
         rng = np.random.default_rng([spec.seed, 1, c0 // _CHUNK_ROWS])
         n = c1 - c0
+        if spec.dist == "unique":
+            # every element a distinct finite code (layout checks); squares stay finite
+            idx = (np.arange(c0, c1, dtype=np.int64)[:, None] * ncols
+                   + np.arange(ncols, dtype=np.int64)[None, :])
+            top = 0x7BFF if spec.in_dtype == FP16 else 0x46FF
+            qkv[c0:c1, :ncols] = (idx % top + 1).astype(np.uint16)
+            return
         if spec.dist == "normal":
             x = rng.standard_normal((n, ncols), dtype=np.float32)
         elif spec.dist == "zeros":
@@ -171,21 +182,20 @@ def generate(spec: Spec) -> Inputs:
             # magnitudes around the 16-bit subnormal range
             lo = 2.0 ** -24 if spec.in_dtype == FP16 else 2.0 ** -133
             x = (rng.uniform(-64, 64, (n, ncols)) * lo).astype(np.float32)
-        elif spec.dist == "unique":
-            # every element a distinct small integer code (layout checks)
-            x = None
         else:
             raise ValueError(spec.dist)
-        if x is None:
-            idx = (np.arange(c0, c1, dtype=np.int64)[:, None] * ncols
-                   + np.arange(ncols, dtype=np.int64)[None, :])
-            top = 0x7BFF if spec.in_dtype == FP16 else 0x46FF   # finite, squares stay finite
-            codes = (idx % top + 1).astype(np.uint16)
-            qkv[c0:c1, :ncols] = codes
-            continue
         if n_out:
             x[:, cols] *= np.float32(spec.outlier_scale)
         qkv[c0:c1, :ncols] = _to16(x, spec.in_dtype)
+
+    starts = list(range(0, spec.rows, _CHUNK_ROWS))
+    if len(starts) > 2:
+        workers = max(1, min(16, os.cpu_count() or 1))
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(fill, starts))
+    else:
+        for c0 in starts:
+            fill(c0)
     return Inputs(spec, qkv, wq, wk, positions(spec), static, cols)
 
 
