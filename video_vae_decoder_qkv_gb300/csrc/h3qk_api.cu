@@ -51,40 +51,45 @@ int next_pow2(int v)
     return p;
 }
 
-template <bool BF16, int LPR>
+template <bool BF16, int LPR, int CH>
 cudaError_t launch_mode(int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
 {
+    constexpr int U = h3qk::kUnroll;
+    constexpr bool PIPE = h3qk::kPipe;
     switch (mode) {
     case h3qk::kOut16:
-        h3qk::qkprep_kernel<BF16, LPR, h3qk::kOut16><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        h3qk::qkprep_kernel<BF16, LPR, CH, U, PIPE, h3qk::kOut16><<<blocks, h3qk::kThreads, 0, st>>>(p);
         break;
     case h3qk::kAmax:
-        h3qk::qkprep_kernel<BF16, LPR, h3qk::kAmax><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        h3qk::qkprep_kernel<BF16, LPR, CH, U, PIPE, h3qk::kAmax><<<blocks, h3qk::kThreads, 0, st>>>(p);
         break;
     default:
-        h3qk::qkprep_kernel<BF16, LPR, h3qk::kCast><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        h3qk::qkprep_kernel<BF16, LPR, CH, U, PIPE, h3qk::kCast><<<blocks, h3qk::kThreads, 0, st>>>(p);
         break;
     }
     ++g_launches;
     return cudaGetLastError();
 }
 
+// P = next_pow2(D/8) chunk slots per head row: CH per lane on P/CH lanes.
 template <bool BF16>
-cudaError_t launch_lpr(int lpr, int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
+cudaError_t launch_p(int P, int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
 {
-    switch (lpr) {
-    case 1: return launch_mode<BF16, 1>(mode, p, blocks, st);
-    case 2: return launch_mode<BF16, 2>(mode, p, blocks, st);
-    case 4: return launch_mode<BF16, 4>(mode, p, blocks, st);
-    case 8: return launch_mode<BF16, 8>(mode, p, blocks, st);
-    case 16: return launch_mode<BF16, 16>(mode, p, blocks, st);
-    default: return launch_mode<BF16, 32>(mode, p, blocks, st);
+    constexpr int CH = h3qk::kChunksPerLane;
+    if (P < CH) return launch_mode<BF16, 1, 1>(mode, p, blocks, st);   // D = 8 with CH > 1
+    switch (P / CH) {
+    case 1: return launch_mode<BF16, 1, CH>(mode, p, blocks, st);
+    case 2: return launch_mode<BF16, 2, CH>(mode, p, blocks, st);
+    case 4: return launch_mode<BF16, 4, CH>(mode, p, blocks, st);
+    case 8: return launch_mode<BF16, 8, CH>(mode, p, blocks, st);
+    case 16: return launch_mode<BF16, 16, CH>(mode, p, blocks, st);
+    default: return launch_mode<BF16, 32 / CH, CH>(mode, p, blocks, st);
     }
 }
 
-cudaError_t launch(bool bf16, int lpr, int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
+cudaError_t launch(bool bf16, int P, int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
 {
-    return bf16 ? launch_lpr<true>(lpr, mode, p, blocks, st) : launch_lpr<false>(lpr, mode, p, blocks, st);
+    return bf16 ? launch_p<true>(P, mode, p, blocks, st) : launch_p<false>(P, mode, p, blocks, st);
 }
 
 h3qk_status fail_cuda(cudaError_t e)
@@ -262,7 +267,8 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
             p.axis[pair] = static_cast<uint8_t>(a);
         }
 
-    const int lpr = next_pow2(head_dim / 8);
+    const int P = next_pow2(head_dim / 8);
+    const int lpr = P < h3qk::kChunksPerLane ? 1 : P / h3qk::kChunksPerLane;
     const int64_t tpw = 32 / lpr;
     const int64_t groups = (tokens + tpw - 1) / tpw;
     const int64_t want = (groups + h3qk::kWarpsPerBlock - 1) / h3qk::kWarpsPerBlock;
@@ -274,7 +280,7 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
 
     if (!e4m3) {
         if (tokens == 0 || valid_len == 0) return H3QK_OK;
-        e = launch(bf16, lpr, h3qk::kOut16, p, blocks, st);
+        e = launch(bf16, P, h3qk::kOut16, p, blocks, st);
         return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
     }
     if (scale_mode == H3QK_SCALE_DYNAMIC) {
@@ -282,11 +288,11 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
         ++g_launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return fail_cuda(e);
         if (tokens > 0 && valid_len > 0) {
-            e = launch(bf16, lpr, h3qk::kAmax, p, blocks, st);
+            e = launch(bf16, P, h3qk::kAmax, p, blocks, st);
             if (e != cudaSuccess) return fail_cuda(e);
         }
     }
-    e = launch(bf16, lpr, h3qk::kCast, p, blocks, st);
+    e = launch(bf16, P, h3qk::kCast, p, blocks, st);
     return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
 }
 

@@ -33,7 +33,25 @@ namespace h3qk {
 constexpr int kMaxPairs = 128;       // rotary_dim <= 256
 constexpr int kWarpsPerBlock = 8;
 constexpr int kThreads = 32 * kWarpsPerBlock;
-constexpr int kUnroll = 4;           // head rows in flight per warp
+// Tuning knobs (compile-time; the defaults are the measured best):
+// H3QK_CH chunks of 8 channels per lane, H3QK_UNROLL head rows per batch,
+// H3QK_PIPE prefetch of the next batch, H3QK_MIN_BLOCKS resident blocks per SM
+// asked of the register allocator.
+#ifndef H3QK_CH
+#define H3QK_CH 1
+#endif
+#ifndef H3QK_UNROLL
+#define H3QK_UNROLL 4
+#endif
+#ifndef H3QK_PIPE
+#define H3QK_PIPE 0
+#endif
+#ifndef H3QK_MIN_BLOCKS
+#define H3QK_MIN_BLOCKS 1
+#endif
+constexpr int kChunksPerLane = H3QK_CH;
+constexpr int kUnroll = H3QK_UNROLL;
+constexpr bool kPipe = H3QK_PIPE != 0;
 
 enum Mode : int { kOut16 = 0, kAmax = 1, kCast = 2 };
 
@@ -148,19 +166,50 @@ __device__ __forceinline__ uint4 load16(const uint16_t* p)
 }
 
 // ---------------------------------------------------------------------------
-// The kernel: each warp walks groups of 32/LPR token rows (grid-stride) and,
-// for each row, the 3*H head rows Q[0..H), K[0..H), V[0..H) kUnroll at a time.
+// The kernel.  A head row's C = D/8 chunks (8 channels = 16 bytes each) sit
+// on LPR lanes, CH chunks per lane (chunks c, c+LPR, ..., LPR*CH =
+// next_pow2(C)); a warp covers TPW = 32/LPR token rows.  Each warp walks
+// groups of TPW rows (grid-stride) and, for each, the 3*H head rows
+// Q[0..H), K[0..H), V[0..H) in batches of U, optionally loading the next
+// batch before computing the current one (PIPE).  The reduction tree is the
+// same for every (LPR, CH): the first log2(CH) halving levels pair chunks
+// held by the same lane, the rest are xor shuffles.
 // MODE kOut16 writes 16-bit head-major outputs; kAmax reduces max |y| per
 // tensor; kCast writes e4m3 codes under the dynamic or static factors.
 // ---------------------------------------------------------------------------
-template <bool BF16, int LPR, int MODE>
-__global__ void __launch_bounds__(kThreads) qkprep_kernel(const __grid_constant__ Params p)
+template <int CH, int U>
+struct Batch {
+    uint4 v[U][CH];
+};
+
+template <int LPR, int CH, int U>
+__device__ __forceinline__ void load_batch(Batch<CH, U>& bt, const uint16_t* row, int j0, int H,
+                                           int D, int64_t HD, const bool (&act)[CH])
+{
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int j = j0 + u;
+        const int part = j / H;
+        const int h = j - part * H;
+        const bool in = j < 3 * H;
+#pragma unroll
+        for (int q = 0; q < CH; ++q) {
+            bt.v[u][q] = make_uint4(0u, 0u, 0u, 0u);
+            if (in && act[q]) bt.v[u][q] = load16(row + part * HD + static_cast<int64_t>(h) * D + 8 * q * LPR);
+        }
+    }
+}
+
+template <bool BF16, int LPR, int CH, int U, bool PIPE, int MODE>
+__global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const __grid_constant__ Params p)
 {
     constexpr int TPW = 32 / LPR;
     const int lane = threadIdx.x & 31;
     const int sub = lane / LPR;
     const int c = lane % LPR;
-    const bool chunk_on = c < p.chunks;
+    bool chunk_on[CH];
+#pragma unroll
+    for (int q = 0; q < CH; ++q) chunk_on[q] = c + q * LPR < p.chunks;
     const int H = p.heads;
     const int D = p.head_dim;
     const int64_t HD = static_cast<int64_t>(H) * D;
@@ -192,19 +241,22 @@ __global__ void __launch_bounds__(kThreads) qkprep_kernel(const __grid_constant_
         }
     }
 
-    // This lane's 8 norm weights of Q and K.
-    float wq[8], wk[8];
-    if (chunk_on) {
-        const float4* q4 = reinterpret_cast<const float4*>(p.wq + 8 * c);
-        const float4* k4 = reinterpret_cast<const float4*>(p.wk + 8 * c);
-        float4 a = __ldg(q4), b = __ldg(q4 + 1), e = __ldg(k4), f = __ldg(k4 + 1);
-        wq[0] = a.x; wq[1] = a.y; wq[2] = a.z; wq[3] = a.w;
-        wq[4] = b.x; wq[5] = b.y; wq[6] = b.z; wq[7] = b.w;
-        wk[0] = e.x; wk[1] = e.y; wk[2] = e.z; wk[3] = e.w;
-        wk[4] = f.x; wk[5] = f.y; wk[6] = f.z; wk[7] = f.w;
-    } else {
+    // This lane's norm weights of Q and K, 8 per chunk.
+    float wq[CH][8], wk[CH][8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) wq[k] = wk[k] = 0.0f;
+    for (int q = 0; q < CH; ++q) {
+        if (chunk_on[q]) {
+            const float4* q4 = reinterpret_cast<const float4*>(p.wq + 8 * (c + q * LPR));
+            const float4* k4 = reinterpret_cast<const float4*>(p.wk + 8 * (c + q * LPR));
+            const float4 a = __ldg(q4), b = __ldg(q4 + 1), e = __ldg(k4), f = __ldg(k4 + 1);
+            wq[q][0] = a.x; wq[q][1] = a.y; wq[q][2] = a.z; wq[q][3] = a.w;
+            wq[q][4] = b.x; wq[q][5] = b.y; wq[q][6] = b.z; wq[q][7] = b.w;
+            wk[q][0] = e.x; wk[q][1] = e.y; wk[q][2] = e.z; wk[q][3] = e.w;
+            wk[q][4] = f.x; wk[q][5] = f.y; wk[q][6] = f.z; wk[q][7] = f.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) wq[q][k] = wk[q][k] = 0.0f;
+        }
     }
 
     float amax[3] = {0.0f, 0.0f, 0.0f};
@@ -212,117 +264,141 @@ __global__ void __launch_bounds__(kThreads) qkprep_kernel(const __grid_constant_
     for (int64_t g = warp0; g < n_groups; g += n_warps) {
         const int64_t r = g * TPW + sub;
         int64_t b = 0, s = 0;
-        bool act = false;
+        bool act_row = false;
         if (r < p.rows) {
             b = r / p.seq;
             s = r - b * p.seq;
-            act = chunk_on && s < p.valid_len;
+            act_row = s < p.valid_len;
         }
-
-        // Rotary cos/sin of this lane's 4 pairs (pair index 4c + k).
-        float cs[4], sn[4];
-        bool rot[4];
+        bool act[CH];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int pair = 4 * c + k;
-            rot[k] = 2 * pair < p.rotary_dim;
-            cs[k] = 1.0f;
-            sn[k] = 0.0f;
-            if (rot[k] && act) {
-                const float pv = static_cast<float>(__ldg(p.pos + r * p.n_axes + p.axis[pair]));
-                sincos_h3(__fmul_rn(pv, p.inv_freq[pair]), sn[k], cs[k]);
+        for (int q = 0; q < CH; ++q) act[q] = act_row && chunk_on[q];
+
+        // Rotary cos/sin of this lane's pairs (pair index 4*(c + q*LPR) + k).
+        float cs[CH][4], sn[CH][4];
+        bool rot[CH][4];
+#pragma unroll
+        for (int q = 0; q < CH; ++q)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int pair = 4 * (c + q * LPR) + k;
+                rot[q][k] = 2 * pair < p.rotary_dim;
+                cs[q][k] = 1.0f;
+                sn[q][k] = 0.0f;
+                if (rot[q][k] && act[q]) {
+                    const float pv = static_cast<float>(__ldg(p.pos + r * p.n_axes + p.axis[pair]));
+                    sincos_h3(__fmul_rn(pv, p.inv_freq[pair]), sn[q][k], cs[q][k]);
+                }
             }
-        }
 
         const uint16_t* row = p.qkv + r * p.row_stride + 8 * c;
         const int64_t obase = (b * H * p.seq + s) * D + 8 * c;
 
-        for (int j0 = 0; j0 < 3 * H; j0 += kUnroll) {
-            uint4 raw[kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int j = j0 + u;
-                raw[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (act && j < 3 * H) {
-                    const int part = j / H;
-                    const int h = j - part * H;
-                    raw[u] = load16(row + part * HD + static_cast<int64_t>(h) * D);
-                }
+        Batch<CH, U> cur;
+        if constexpr (PIPE) load_batch<LPR, CH, U>(cur, row, 0, H, D, HD, act);
+        for (int j0 = 0; j0 < 3 * H; j0 += U) {
+            Batch<CH, U> nxt;
+            if constexpr (PIPE) {
+                if (j0 + U < 3 * H) load_batch<LPR, CH, U>(nxt, row, j0 + U, H, D, HD, act);
+            } else {
+                load_batch<LPR, CH, U>(cur, row, j0, H, D, HD, act);
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < U; ++u) {
                 const int j = j0 + u;
                 if (j >= 3 * H) break;                 // warp-uniform
                 const int part = j / H;
                 const int h = j - part * H;
-                uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-                uint32_t y[4];
+                uint32_t y[CH][4];
                 if (part < 2) {
-                    float x[8];
+                    float x[CH][8];
+                    float acc[CH];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float2 f = widen2<BF16>(wv[k]);
-                        x[2 * k] = f.x;
-                        x[2 * k + 1] = f.y;
+                    for (int q = 0; q < CH; ++q) {
+                        const uint32_t wv[4] = {cur.v[u][q].x, cur.v[u][q].y, cur.v[u][q].z, cur.v[u][q].w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 f = widen2<BF16>(wv[k]);
+                            x[q][2 * k] = f.x;
+                            x[q][2 * k + 1] = f.y;
+                        }
+                        // Sum of squares of one chunk: 8 channels left to right.
+                        acc[q] = __fmul_rn(x[q][0], x[q][0]);
+#pragma unroll
+                        for (int k = 1; k < 8; ++k) acc[q] = __fadd_rn(acc[q], __fmul_rn(x[q][k], x[q][k]));
                     }
-                    // Sum of squares: 8 channels left to right, then the halving tree.
-                    float acc = __fmul_rn(x[0], x[0]);
+                    // Halving tree: levels pairing chunks of this lane, then shuffles.
 #pragma unroll
-                    for (int k = 1; k < 8; ++k) acc = __fadd_rn(acc, __fmul_rn(x[k], x[k]));
+                    for (int o = CH / 2; o >= 1; o >>= 1)
+#pragma unroll
+                        for (int q = 0; q < o; ++q) acc[q] = __fadd_rn(acc[q], acc[q + o]);
+                    float ss = acc[0];
 #pragma unroll
                     for (int o = LPR / 2; o >= 1; o >>= 1)
-                        acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-                    const float ms = p.inv_d != 0.0f ? __fmul_rn(acc, p.inv_d)
-                                                     : __fdiv_rn(acc, static_cast<float>(D));
+                        ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+                    const float ms = p.inv_d != 0.0f ? __fmul_rn(ss, p.inv_d)
+                                                     : __fdiv_rn(ss, static_cast<float>(D));
                     const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, p.eps)));
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float w0 = part == 0 ? wq[2 * k] : wk[2 * k];
-                        const float w1 = part == 0 ? wq[2 * k + 1] : wk[2 * k + 1];
-                        const float a0 = __fmul_rn(__fmul_rn(x[2 * k], inv), w0);
-                        const float a1 = __fmul_rn(__fmul_rn(x[2 * k + 1], inv), w1);
-                        uint32_t n2 = round2<BF16>(a0, a1);
-                        if (rot[k]) {
-                            const float2 uv = widen2<BF16>(n2);
-                            const float ro = __fsub_rn(__fmul_rn(uv.x, cs[k]), __fmul_rn(uv.y, sn[k]));
-                            const float rv = __fadd_rn(__fmul_rn(uv.x, sn[k]), __fmul_rn(uv.y, cs[k]));
-                            n2 = round2<BF16>(ro, rv);
+                    for (int q = 0; q < CH; ++q)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float w0 = part == 0 ? wq[q][2 * k] : wk[q][2 * k];
+                            const float w1 = part == 0 ? wq[q][2 * k + 1] : wk[q][2 * k + 1];
+                            const float a0 = __fmul_rn(__fmul_rn(x[q][2 * k], inv), w0);
+                            const float a1 = __fmul_rn(__fmul_rn(x[q][2 * k + 1], inv), w1);
+                            uint32_t n2 = round2<BF16>(a0, a1);
+                            if (rot[q][k]) {
+                                const float2 uv = widen2<BF16>(n2);
+                                const float ro = __fsub_rn(__fmul_rn(uv.x, cs[q][k]), __fmul_rn(uv.y, sn[q][k]));
+                                const float rv = __fadd_rn(__fmul_rn(uv.x, sn[q][k]), __fmul_rn(uv.y, cs[q][k]));
+                                n2 = round2<BF16>(ro, rv);
+                            }
+                            y[q][k] = n2;
                         }
-                        y[k] = n2;
-                    }
                 } else {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) y[k] = wv[k];
+                    for (int q = 0; q < CH; ++q) {
+                        y[q][0] = cur.v[u][q].x;
+                        y[q][1] = cur.v[u][q].y;
+                        y[q][2] = cur.v[u][q].z;
+                        y[q][3] = cur.v[u][q].w;
+                    }
                 }
 
-                if (!act) continue;
-                if constexpr (MODE == kOut16) {
-                    uint16_t* dst = static_cast<uint16_t*>(p.out[part]) + obase + h * head_stride;
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(y[0], y[1], y[2], y[3]);
-                } else if constexpr (MODE == kAmax) {
-                    float m = 0.0f;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float2 f = widen2<BF16>(y[k]);
-                        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-                    }
-                    if (part == 0) amax[0] = fmaxf(amax[0], m);
-                    else if (part == 1) amax[1] = fmaxf(amax[1], m);
-                    else amax[2] = fmaxf(amax[2], m);
-                } else {
-                    const float fa = part == 0 ? fac[0] : (part == 1 ? fac[1] : fac[2]);
-                    uint32_t cw[2];
+                for (int q = 0; q < CH; ++q) {
+                    if (!act[q]) continue;
+                    const int64_t off = obase + h * head_stride + 8 * q * LPR;
+                    if constexpr (MODE == kOut16) {
+                        uint16_t* dst = static_cast<uint16_t*>(p.out[part]) + off;
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(y[q][0], y[q][1], y[q][2], y[q][3]);
+                    } else if constexpr (MODE == kAmax) {
+                        float m = 0.0f;
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const float2 f0 = widen2<BF16>(y[2 * k]);
-                        const float2 f1 = widen2<BF16>(y[2 * k + 1]);
-                        cw[k] = e4m3x2(__fmul_rn(f0.x, fa), __fmul_rn(f0.y, fa)) |
-                                (e4m3x2(__fmul_rn(f1.x, fa), __fmul_rn(f1.y, fa)) << 16);
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 f = widen2<BF16>(y[q][k]);
+                            m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+                        }
+                        if (part == 0) amax[0] = fmaxf(amax[0], m);
+                        else if (part == 1) amax[1] = fmaxf(amax[1], m);
+                        else amax[2] = fmaxf(amax[2], m);
+                    } else {
+                        const float fa = part == 0 ? fac[0] : (part == 1 ? fac[1] : fac[2]);
+                        uint32_t cw[2];
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const float2 f0 = widen2<BF16>(y[q][2 * k]);
+                            const float2 f1 = widen2<BF16>(y[q][2 * k + 1]);
+                            cw[k] = e4m3x2(__fmul_rn(f0.x, fa), __fmul_rn(f0.y, fa)) |
+                                    (e4m3x2(__fmul_rn(f1.x, fa), __fmul_rn(f1.y, fa)) << 16);
+                        }
+                        uint8_t* dst = static_cast<uint8_t*>(p.out[part]) + off;
+                        *reinterpret_cast<uint2*>(dst) = make_uint2(cw[0], cw[1]);
                     }
-                    uint8_t* dst = static_cast<uint8_t*>(p.out[part]) + obase + h * head_stride;
-                    *reinterpret_cast<uint2*>(dst) = make_uint2(cw[0], cw[1]);
                 }
             }
+            if constexpr (PIPE) cur = nxt;
         }
     }
 
