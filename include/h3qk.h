@@ -161,6 +161,37 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
                          void* out_k, void* out_v, float* out_scales, const h3qk_opts* opts,
                          h3qk_stream_t stream);
 
+/*
+ * h3qk_prepare_noalloc: h3qk_prepare for callers that cannot allocate device
+ * memory at the point of the call -- for example a plugin inside an inference
+ * engine that receives all of its memory up front, or a real-time decode loop
+ * whose memory budget is fixed at start-up.  The pages have no counterpart to
+ * this entry point; it is a property of this library only.
+ *
+ * Arguments, results and errors are those of h3qk_prepare, except that a
+ * DYNAMIC call ignores opts->workspace and keeps its amax words in a fixed
+ * scratch array inside the library (a file-scope __device__ array of 256
+ * bytes, 256-byte aligned, held by every GPU that loads the library until the
+ * process exits).  A call needs 16 bytes of it whatever its sizes; a call
+ * that needed more than the array holds would be rejected with
+ * H3QK_ERR_INVALID_ARG.  The call allocates nothing and calls no allocating
+ * routine.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and keeps it; make that first call before any stream
+ * capture on that device.  Every call shares the one array, which keeps the
+ * last call's contents (each DYNAMIC call clears its amax words first), so
+ * DYNAMIC calls whose kernels overlap on the GPU (different streams, no
+ * ordering between them) race on it: order them on one stream, or use
+ * h3qk_prepare with a workspace per stream.
+ */
+h3qk_status h3qk_prepare_noalloc(const void* qkv, const float* norm_wq, const float* norm_wk,
+                                 const int32_t* positions, int64_t tokens, int32_t heads,
+                                 int32_t head_dim, int32_t rotary_dim, int64_t valid_len,
+                                 h3qk_dtype out_dtype, h3qk_scale_mode scale_mode, void* out_q,
+                                 void* out_k, void* out_v, float* out_scales,
+                                 const h3qk_opts* opts, h3qk_stream_t stream);
+
 /* A static, human-readable name of a status. */
 const char* h3qk_status_string(h3qk_status status);
 

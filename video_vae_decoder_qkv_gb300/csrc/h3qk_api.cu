@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "h3qk.h"
 #include "h3qk_kernels.cuh"
@@ -297,3 +298,66 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// h3qk_prepare_noalloc: h3qk_prepare for callers that cannot allocate device
+// memory.  Its only scratch is the fixed array below (the three amax words of
+// a DYNAMIC call); every GPU that loads this library holds it until exit.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoallocScratchBytes = 256;
+static __device__ __align__(256) unsigned int g_noalloc_scratch[kNoallocScratchBytes / 4];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {nullptr};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (the host-side name is only a stand-in for the device array).
+h3qk_status noalloc_scratch(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return H3QK_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) return fail_cuda(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return H3QK_OK;
+}
+
+}  // namespace
+
+extern "C" h3qk_status h3qk_prepare_noalloc(const void* qkv, const float* norm_wq,
+                                            const float* norm_wk, const int32_t* positions,
+                                            int64_t tokens, int32_t heads, int32_t head_dim,
+                                            int32_t rotary_dim, int64_t valid_len,
+                                            h3qk_dtype out_dtype, h3qk_scale_mode scale_mode,
+                                            void* out_q, void* out_k, void* out_v,
+                                            float* out_scales, const h3qk_opts* opts,
+                                            h3qk_stream_t stream)
+{
+    h3qk_opts o;
+    h3qk_opts_init(&o);
+    if (opts) o = *opts;
+    if (scale_mode == H3QK_SCALE_DYNAMIC) {
+        // The scratch a call needs must fit the fixed array.  A DYNAMIC call
+        // needs h3qk_workspace_bytes() = 16 bytes whatever its sizes, so this
+        // rejects nothing today; it keeps the limit explicit.
+        if (h3qk_workspace_bytes() > kNoallocScratchBytes) return H3QK_ERR_INVALID_ARG;
+        void* ws = nullptr;
+        const h3qk_status st = noalloc_scratch(&ws);
+        if (st != H3QK_OK) return st;
+        // The kernels clear the amax words at the start of every DYNAMIC call.
+        o.workspace = ws;
+        o.workspace_bytes = kNoallocScratchBytes;
+    }
+    return h3qk_prepare(qkv, norm_wq, norm_wk, positions, tokens, heads, head_dim, rotary_dim,
+                        valid_len, out_dtype, scale_mode, out_q, out_k, out_v, out_scales, &o,
+                        stream);
+}

@@ -113,6 +113,24 @@ def prepare_ptr(qkv, norm_wq, norm_wk, positions, tokens, heads, head_dim, rotar
                               ctypes.byref(opts) if opts is not None else None, stream))
 
 
+def prepare_noalloc_ptr(qkv, norm_wq, norm_wk, positions, tokens, heads, head_dim, rotary_dim,
+                        valid_len, out_dtype, scale_mode, out_q, out_k, out_v, out_scales,
+                        opts: Opts | None, stream) -> int:
+    """Call h3qk_prepare_noalloc (for callers that cannot allocate device
+    memory: a DYNAMIC call keeps its amax words in the library's own fixed
+    scratch array) with raw integer addresses; returns the status."""
+    L = lib()
+    fn = L.h3qk_prepare_noalloc
+    if fn.argtypes is None:
+        P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        fn.restype = ctypes.c_int
+        fn.argtypes = [P, P, P, P, I64, I32, I32, I32, I64, ctypes.c_int, ctypes.c_int,
+                       P, P, P, P, ctypes.POINTER(Opts), P]
+    return int(fn(qkv, norm_wq, norm_wk, positions, int(tokens), int(heads), int(head_dim),
+                  int(rotary_dim), int(valid_len), int(out_dtype), int(scale_mode), out_q, out_k,
+                  out_v, out_scales, ctypes.byref(opts) if opts is not None else None, stream))
+
+
 def _ptr(t):
     return None if t is None else t.data_ptr()
 
