@@ -162,6 +162,44 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
                          h3qk_stream_t stream);
 
 /*
+ * h3qk_amax and h3qk_cast: the two passes of a DYNAMIC e4m3 call, separately,
+ * so that a caller whose rows are sharded over several GPUs can all-reduce
+ * (MAX) the three amax values between them and cast every shard with the
+ * same scales.  This is the exchange the pages make under Ulysses sequence
+ * parallelism (TensorRT-LLM PR #21485, commit on the amax all-reduce: "every
+ * rank casts and dequantizes with the same scale").  On one GPU,
+ * h3qk_amax followed by h3qk_cast on the same stream gives the same bytes as
+ * h3qk_prepare with H3QK_SCALE_DYNAMIC.
+ *
+ * The input arguments are those of h3qk_prepare; opts->in_dtype DEFAULT means
+ * BF16 here, and opts->static_scales / workspace are ignored.
+ *
+ * h3qk_amax writes out_amax (device float[3], 4-byte aligned): the largest
+ * |y| of Q, K and V over the valid rows, y the 16-bit value h3qk_prepare
+ * would write (0 when no row is valid).  It zeroes out_amax first, on the
+ * stream, then accumulates into it with atomics.
+ *
+ * h3qk_cast reads amax (device float[3]; after any all-reduce), derives the
+ * dynamic scales from it as h3qk_prepare does (scale = amax / 448, factor =
+ * 448 / amax; 1 and 1 for a zero, subnormal, infinite or NaN amax) and writes
+ * the e4m3 codes of the valid rows into out_q, out_k, out_v and the three
+ * descales into out_scales.  Outputs must not overlap the inputs, amax or
+ * each other.
+ *
+ * Errors and asynchrony as for h3qk_prepare.
+ */
+h3qk_status h3qk_amax(const void* qkv, const float* norm_wq, const float* norm_wk,
+                      const int32_t* positions, int64_t tokens, int32_t heads, int32_t head_dim,
+                      int32_t rotary_dim, int64_t valid_len, float* out_amax, const h3qk_opts* opts,
+                      h3qk_stream_t stream);
+
+h3qk_status h3qk_cast(const void* qkv, const float* norm_wq, const float* norm_wk,
+                      const int32_t* positions, int64_t tokens, int32_t heads, int32_t head_dim,
+                      int32_t rotary_dim, int64_t valid_len, const float* amax, void* out_q,
+                      void* out_k, void* out_v, float* out_scales, const h3qk_opts* opts,
+                      h3qk_stream_t stream);
+
+/*
  * h3qk_prepare_noalloc: h3qk_prepare for callers that cannot allocate device
  * memory at the point of the call -- for example a plugin inside an inference
  * engine that receives all of its memory up front, or a real-time decode loop

@@ -107,6 +107,7 @@ class Problem:
     eps: float = 1e-6
     theta: float = 10000.0
     static_scales: tuple = (1.0, 1.0, 1.0)
+    tensor: bool = False   # one [B, S, H, D] tensor instead of packed QKV rows
 
     def __post_init__(self):
         if not self.axis_dims:
@@ -117,7 +118,7 @@ class Problem:
         if self.valid_len is None:
             self.valid_len = self.seq
         if self.row_stride is None:
-            self.row_stride = 3 * self.heads * self.head_dim
+            self.row_stride = (1 if self.tensor else 3) * self.heads * self.head_dim
         self.check()
 
     @property
@@ -142,8 +143,8 @@ class Problem:
             raise ValueError("heads * head_dim too large for the oracle")
         if not (0 <= self.valid_len <= self.seq):
             raise ValueError("valid_len must lie in [0, seq]")
-        if self.row_stride < 3 * self.hd:
-            raise ValueError("row_stride shorter than a packed row")
+        if self.row_stride < (1 if self.tensor else 3) * self.hd:
+            raise ValueError("row_stride shorter than a row")
 
     def c(self) -> _Problem:
         p = _Problem()
@@ -197,6 +198,10 @@ def lib():
                 "h3o_cast_row": (None, [PP, _P, _P, _P, _P, _I64, _P, _P, _P, _P]),
                 "h3o_prepare": (None, [PP, _P, _P, _P, _P, _P, _P, _P, _P]),
                 "h3o_angles_array": (None, [PP, _P, _I64, _P]),
+                "h3o_tensor_row16": (None, [PP, ctypes.c_int, _P, _P, _P, _I64, _P]),
+                "h3o_tensor16_rows": (None, [PP, ctypes.c_int, _P, _P, _P, _I64, _I64, _P]),
+                "h3o_tensor_amax_rows": (ctypes.c_float, [PP, ctypes.c_int, _P, _P, _P, _I64, _I64]),
+                "h3o_tensor_cast_rows": (None, [PP, ctypes.c_int, _P, _P, _P, _I64, _I64, ctypes.c_float, _P]),
                 "h3o_problem_inv_freq_public": (None, [PP, _P]),
             }
             for name, (res, args) in sigs.items():
@@ -418,3 +423,40 @@ def f16_to_f32(codes) -> np.ndarray:
 def bf16_to_f32(codes) -> np.ndarray:
     """bfloat16 codes -> float32 (exact: the codes are the upper 16 bits)."""
     return (np.asarray(codes, np.uint32) << 16).astype(np.uint32).view(np.float32)
+
+
+# --------------------------------------------------------------------------
+# The single-tensor variant: one [B, S, H, D] tensor, norm + RoPE (kind 0 Q,
+# 1 K) or identity (kind 2 V), token-major output.
+# --------------------------------------------------------------------------
+
+def tensor_prepare(pb: Problem, kind: int, x, w, pos, out=None, threads: int = 1):
+    """Returns (out, scale): token-major [B, S, H, D] uint16 codes (16-bit
+    mode) or uint8 e4m3 codes and the one descale (None in 16-bit mode).
+    Rows past valid_len keep the contents of ``out``."""
+    assert pb.tensor, "tensor_prepare needs Problem(tensor=True)"
+    x = _c(x, np.uint16)
+    if x.ndim != 2 or x.shape != (pb.rows, pb.row_stride):
+        raise ValueError(f"x must be uint16 [{pb.rows}, {pb.row_stride}]")
+    w = _c(w if w is not None else np.zeros(pb.head_dim, np.float32), np.float32)
+    pos = _c(pos, np.int32)
+    shape = (pb.batch, pb.seq, pb.heads, pb.head_dim)
+    odt = np.uint16 if pb.out_kind == OUT_16B else np.uint8
+    if out is None:
+        out = np.zeros(shape, odt)
+    assert out.dtype == odt and out.shape == shape and out.flags.c_contiguous
+    L, cp = lib(), pb.c()
+    args = (ctypes.byref(cp), int(kind), _ptr(x), _ptr(w), _ptr(pos))
+    parts = _ranges(pb.rows, threads)
+    with ThreadPoolExecutor(max(1, threads)) as ex:
+        if pb.out_kind == OUT_16B:
+            list(ex.map(lambda rg: L.h3o_tensor16_rows(*args, rg[0], rg[1], _ptr(out)), parts))
+            return out, None
+        am = 0.0
+        if pb.scale_mode == SCALE_DYNAMIC:
+            am = max([0.0] + list(ex.map(lambda rg: L.h3o_tensor_amax_rows(*args, rg[0], rg[1]), parts)))
+        sc, inv = scales(pb, np.array([am, am, am], np.float32))
+        k = 0 if pb.scale_mode == SCALE_STATIC else 0
+        scale, factor = float(sc[k]), float(inv[k])
+        list(ex.map(lambda rg: L.h3o_tensor_cast_rows(*args, rg[0], rg[1], factor, _ptr(out)), parts))
+    return out, np.float32(scale)

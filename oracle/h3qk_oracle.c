@@ -617,6 +617,80 @@ void h3o_prepare(const h3o_problem* pb, const uint16_t* qkv, const float* wq, co
 }
 
 /* ------------------------------------------------------------------------ */
+/* Single-tensor variant [P2 norm_rope_tensor commit: one [B, S, H, D]       */
+/* tensor, norm + RoPE for Q / K, identity for V, to 16 bits or e4m3 with   */
+/* its own per-tensor descale].  x holds rows of H*D values (row stride     */
+/* pb->row_stride); kind 0 = Q, 1 = K (normalised with w, rotated), 2 = V   */
+/* (copied).  The output is token-major [B, S, H, D], the layout of the     */
+/* input.                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* The 16-bit values of row r of the tensor (H*D, head by head). */
+void h3o_tensor_row16(const h3o_problem* pb, int kind, const uint16_t* x, const float* w,
+                      const int32_t* pos, int64_t r, uint16_t* y)
+{
+    const int H = pb->heads, D = pb->head_dim, R = pb->rotary_dim;
+    const uint16_t* row = x + r * pb->row_stride;
+    if (kind == 2) {
+        for (int64_t e = 0; e < (int64_t)H * D; ++e) y[e] = row[e];
+        return;
+    }
+    float inv_freq[H3O_MAX_PAIRS], cs[H3O_MAX_PAIRS], sn[H3O_MAX_PAIRS], xf[256];
+    uint16_t n[256];
+    h3o_problem_inv_freq(pb, inv_freq);
+    h3o_token_angles(pb, pos + r * pb->n_axes, inv_freq, cs, sn);
+    for (int h = 0; h < H; ++h) {
+        const uint16_t* src = row + (int64_t)h * D;
+        for (int d = 0; d < D; ++d) xf[d] = h3o_widen(pb->in_dtype, src[d]);
+        h3o_norm_head(pb->in_dtype, xf, w, D, pb->eps, n);
+        uint16_t* dst = y + (int64_t)h * D;
+        for (int i = 0; i < R / 2; ++i)
+            h3o_rotate_pair(pb->in_dtype, cs[i], sn[i], n[2 * i], n[2 * i + 1], &dst[2 * i], &dst[2 * i + 1]);
+        for (int d = R; d < D; ++d) dst[d] = n[d];
+    }
+}
+
+/* 16-bit output of the valid rows in [row0, row1), token-major. */
+void h3o_tensor16_rows(const h3o_problem* pb, int kind, const uint16_t* x, const float* w,
+                       const int32_t* pos, int64_t row0, int64_t row1, uint16_t* out)
+{
+    const int64_t HD = (int64_t)pb->heads * pb->head_dim;
+    for (int64_t r = row0; r < row1; ++r)
+        if (h3o_row_valid(pb, r)) h3o_tensor_row16(pb, kind, x, w, pos, r, out + r * HD);
+}
+
+/* amax over the valid rows in [row0, row1) of the tensor's 16-bit values. */
+float h3o_tensor_amax_rows(const h3o_problem* pb, int kind, const uint16_t* x, const float* w,
+                           const int32_t* pos, int64_t row0, int64_t row1)
+{
+    const int64_t HD = (int64_t)pb->heads * pb->head_dim;
+    uint16_t y[H3O_MAX_HD];
+    float m = 0.0f;
+    for (int64_t r = row0; r < row1; ++r) {
+        if (!h3o_row_valid(pb, r)) continue;
+        h3o_tensor_row16(pb, kind, x, w, pos, r, y);
+        for (int64_t e = 0; e < HD; ++e) {
+            float a = fabsf(h3o_widen(pb->in_dtype, y[e]));
+            if (a > m) m = a;
+        }
+    }
+    return m;
+}
+
+/* e4m3 codes of the valid rows in [row0, row1), token-major, under factor inv. */
+void h3o_tensor_cast_rows(const h3o_problem* pb, int kind, const uint16_t* x, const float* w,
+                          const int32_t* pos, int64_t row0, int64_t row1, float inv, uint8_t* out)
+{
+    const int64_t HD = (int64_t)pb->heads * pb->head_dim;
+    uint16_t y[H3O_MAX_HD];
+    for (int64_t r = row0; r < row1; ++r) {
+        if (!h3o_row_valid(pb, r)) continue;
+        h3o_tensor_row16(pb, kind, x, w, pos, r, y);
+        h3o_cast_values(pb->in_dtype, y, HD, inv, out + r * HD);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Array helpers for the tests (element-wise loops over the scalar steps).  */
 /* ------------------------------------------------------------------------ */
 

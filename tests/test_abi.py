@@ -117,3 +117,35 @@ def test_valid_call_without_a_device_reports_cuda_error():
         pytest.skip("a GPU is present; the fake addresses must not reach a launch")
     assert call() == h3qk.ERR_CUDA
     assert h3qk.lib().h3qk_last_cuda_error() != 0
+
+
+def _split_call(fn, **kw):
+    import ctypes as C
+
+    L = h3qk.lib()
+    h3qk._split_sigs(L)
+    a = dict(qkv=QKV, norm_wq=WQ, norm_wk=WK, positions=POS, tokens=N, heads=H, head_dim=D,
+             rotary_dim=R, valid_len=N)
+    a.update({k: v for k, v in kw.items() if k in a})
+    args = [a["qkv"], a["norm_wq"], a["norm_wk"], a["positions"], a["tokens"], a["heads"], a["head_dim"],
+            a["rotary_dim"], a["valid_len"]]
+    if fn == "amax":
+        return L.h3qk_amax(*args, kw.get("out_amax", SC), None, None)
+    return L.h3qk_cast(*args, kw.get("amax", TAB), kw.get("out_q", OQ), kw.get("out_k", OK_),
+                       kw.get("out_v", OV), kw.get("out_scales", SC), None, None)
+
+
+@pytest.mark.parametrize("fn,kw,want", [
+    ("amax", dict(out_amax=None), h3qk.ERR_INVALID_ARG),
+    ("amax", dict(out_amax=SC + 2), h3qk.ERR_MISALIGNED),
+    ("amax", dict(out_amax=QKV + 64), h3qk.ERR_ALIAS),
+    ("amax", dict(head_dim=12), h3qk.ERR_INVALID_ARG),
+    ("cast", dict(amax=None), h3qk.ERR_INVALID_ARG),
+    ("cast", dict(out_scales=None), h3qk.ERR_INVALID_ARG),
+    ("cast", dict(out_k=OQ), h3qk.ERR_ALIAS),
+    ("cast", dict(out_scales=TAB), h3qk.ERR_ALIAS),
+    ("cast", dict(out_q=OQ + 4), h3qk.ERR_MISALIGNED),
+    ("cast", dict(valid_len=N + 1), h3qk.ERR_INVALID_ARG),
+])
+def test_split_entry_points_check_arguments(fn, kw, want):
+    assert _split_call(fn, **kw) == want

@@ -136,7 +136,7 @@ def test_head_dims_and_rotary_splits(head_dim, rotary_dim, n_axes, axis_dims, dt
     _roundtrip(spec.with_(out_kind=W.OUT_E4M3, scale_mode=W.SCALE_DYNAMIC))
 
 
-@pytest.mark.parametrize("dist", ["zeros", "huge", "tiny", "unique"])
+@pytest.mark.parametrize("dist", ["zeros", "huge", "tiny", "subsq", "unique"])
 @pytest.mark.parametrize("dtype", [W.FP16, W.BF16])
 @pytest.mark.parametrize("mode", ["16b", "dynamic", "static"])
 def test_value_distributions(dist, dtype, mode):
@@ -275,7 +275,7 @@ def _stress_cases(n=64):
         mode = ["16b", "dynamic", "static"][i % 3]
         kw = {"16b": {}, "dynamic": dict(out_kind=W.OUT_E4M3, scale_mode=W.SCALE_DYNAMIC),
               "static": dict(out_kind=W.OUT_E4M3, scale_mode=W.SCALE_STATIC)}[mode]
-        dist = ["normal", "normal", "huge", "tiny", "zeros", "unique"][int(rng.integers(0, 6))]
+        dist = ["normal", "normal", "huge", "tiny", "zeros", "unique", "subsq"][int(rng.integers(0, 7))]
         cases.append(W.Spec(f"stress{i}", batch=B, seq=S, heads=H, head_dim=D, rotary_dim=R,
                             n_axes=n_axes, axis_dims=dims, grid=(1, 1, S) if n_axes == 3 else None,
                             in_dtype=[W.FP16, W.BF16][i % 2], valid_len=int(rng.integers(0, S + 1)),

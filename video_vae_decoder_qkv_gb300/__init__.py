@@ -6,6 +6,6 @@ e4m3 cast (dynamic or static scales, valid-prefix mask).
 The path is libh3qk.so (hand-written sm_103a CUDA behind the C-ABI in
 include/h3qk.h); ``prepare`` is its thin Python binding.
 """
-from .h3qk import H3QKError, prepare  # noqa: F401
+from .h3qk import H3QKError, amax, cast, prepare, prepare_dynamic_sharded  # noqa: F401
 
-__all__ = ["prepare", "H3QKError"]
+__all__ = ["prepare", "amax", "cast", "prepare_dynamic_sharded", "H3QKError"]

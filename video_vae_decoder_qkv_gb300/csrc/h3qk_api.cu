@@ -56,28 +56,31 @@ template <bool BF16, int LPR, int CH>
 cudaError_t launch_mode(int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
 {
     constexpr int U = h3qk::kUnroll;
-    constexpr bool PIPE = h3qk::kPipe;
     switch (mode) {
     case h3qk::kOut16:
-        h3qk::qkprep_kernel<BF16, LPR, CH, U, PIPE, h3qk::kOut16><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        h3qk::qkprep_kernel<BF16, LPR, CH, U, h3qk::kOut16><<<blocks, h3qk::kThreads, 0, st>>>(p);
         break;
     case h3qk::kAmax:
-        h3qk::qkprep_kernel<BF16, LPR, CH, U, PIPE, h3qk::kAmax><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        h3qk::qkprep_kernel<BF16, LPR, CH, U, h3qk::kAmax><<<blocks, h3qk::kThreads, 0, st>>>(p);
         break;
     default:
-        h3qk::qkprep_kernel<BF16, LPR, CH, U, PIPE, h3qk::kCast><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        h3qk::qkprep_kernel<BF16, LPR, CH, U, h3qk::kCast><<<blocks, h3qk::kThreads, 0, st>>>(p);
         break;
     }
     ++g_launches;
     return cudaGetLastError();
 }
 
-// P = next_pow2(D/8) chunk slots per head row: CH per lane on P/CH lanes.
+// P = next_pow2(D/8) chunk slots per head row: CH per lane on P/CH lanes
+// (fewer per lane when P < CH).
 template <bool BF16>
 cudaError_t launch_p(int P, int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
 {
     constexpr int CH = h3qk::kChunksPerLane;
-    if (P < CH) return launch_mode<BF16, 1, 1>(mode, p, blocks, st);   // D = 8 with CH > 1
+    if (P < CH) {
+        if (P == 1) return launch_mode<BF16, 1, 1>(mode, p, blocks, st);
+        return launch_mode<BF16, 1, 2>(mode, p, blocks, st);  // P == 2 < CH == 4
+    }
     switch (P / CH) {
     case 1: return launch_mode<BF16, 1, CH>(mode, p, blocks, st);
     case 2: return launch_mode<BF16, 2, CH>(mode, p, blocks, st);
@@ -137,18 +140,30 @@ void h3qk_launch_count_reset(void) { g_launches = 0; }
 
 int h3qk_version(void) { return 100; }
 
-h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* norm_wk,
-                         const int32_t* positions, int64_t tokens, int32_t heads,
-                         int32_t head_dim, int32_t rotary_dim, int64_t valid_len,
-                         h3qk_dtype out_dtype, h3qk_scale_mode scale_mode, void* out_q,
-                         void* out_k, void* out_v, float* out_scales, const h3qk_opts* opts,
-                         h3qk_stream_t stream)
-{
-    h3qk_opts o;
-    h3qk_opts_init(&o);
-    if (opts) o = *opts;
+}  // extern "C"
 
-    // ---- sizes and options -------------------------------------------------
+namespace {
+
+// One checked call: the kernel parameters, the launch geometry and the byte
+// ranges of the inputs (for the aliasing checks of the outputs).
+struct Plan {
+    h3qk::Params p;
+    bool bf16 = false;
+    int P = 1;
+    int blocks = 1;
+    cudaStream_t st = nullptr;
+    Range ins[4];  // qkv, norm_wq, norm_wk, positions
+    int64_t HD = 0;
+};
+
+// Checks of everything that describes the input rows (sizes, options, input
+// pointers and their alignment) and the launch plan.  `default_in` is the
+// input type assumed when opts->in_dtype is DEFAULT.
+h3qk_status plan_inputs(const void* qkv, const float* norm_wq, const float* norm_wk,
+                        const int32_t* positions, int64_t tokens, int32_t heads, int32_t head_dim,
+                        int32_t rotary_dim, int64_t valid_len, int default_in, const h3qk_opts& o,
+                        h3qk_stream_t stream, Plan* plan)
+{
     if (tokens < 0 || heads < 1 || heads > 65536) return H3QK_ERR_INVALID_ARG;
     if (head_dim < 8 || head_dim > 256 || head_dim % 8) return H3QK_ERR_INVALID_ARG;
     if (rotary_dim < 0 || rotary_dim > head_dim || rotary_dim % 2) return H3QK_ERR_INVALID_ARG;
@@ -174,18 +189,8 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
     if (dim_sum != rotary_dim) return H3QK_ERR_INVALID_ARG;
     if (!(o.eps >= 0.0f) || !std::isfinite(o.eps)) return H3QK_ERR_INVALID_ARG;
     if (!(o.theta > 0.0) || !std::isfinite(o.theta)) return H3QK_ERR_INVALID_ARG;
-
-    int in_dtype = o.in_dtype;
-    if (in_dtype == H3QK_DTYPE_DEFAULT) in_dtype = (out_dtype == H3QK_FP16) ? H3QK_FP16 : H3QK_BF16;
+    int in_dtype = o.in_dtype == H3QK_DTYPE_DEFAULT ? default_in : o.in_dtype;
     if (in_dtype != H3QK_FP16 && in_dtype != H3QK_BF16) return H3QK_ERR_INVALID_ARG;
-    const bool e4m3 = out_dtype == H3QK_E4M3;
-    if (out_dtype == H3QK_FP16 || out_dtype == H3QK_BF16) {
-        if (out_dtype != in_dtype || scale_mode != H3QK_SCALE_NONE) return H3QK_ERR_INVALID_ARG;
-    } else if (e4m3) {
-        if (scale_mode != H3QK_SCALE_DYNAMIC && scale_mode != H3QK_SCALE_STATIC) return H3QK_ERR_INVALID_ARG;
-    } else {
-        return H3QK_ERR_INVALID_ARG;
-    }
 
     const int64_t HD = static_cast<int64_t>(heads) * head_dim;
     const int64_t stride = o.qkv_row_stride ? o.qkv_row_stride : 3 * HD;
@@ -194,59 +199,27 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
     if (tokens > 0 && (stride > (INT64_C(1) << 40) / tokens || HD > (INT64_C(1) << 40) / tokens))
         return H3QK_ERR_INVALID_ARG;
 
-    // ---- pointers ----------------------------------------------------------
     // An empty call (tokens == 0) reads and writes no row, so its row buffers
     // may be NULL (an empty torch tensor has a null data pointer).
     if (!norm_wq || !norm_wk) return H3QK_ERR_INVALID_ARG;
-    if (tokens > 0 && (!qkv || !out_q || !out_k || !out_v)) return H3QK_ERR_INVALID_ARG;
+    if (tokens > 0 && !qkv) return H3QK_ERR_INVALID_ARG;
     if (tokens > 0 && rotary_dim > 0 && !positions) return H3QK_ERR_INVALID_ARG;
-    if (e4m3 && !out_scales) return H3QK_ERR_INVALID_ARG;
-    if (e4m3 && scale_mode == H3QK_SCALE_STATIC && !o.static_scales) return H3QK_ERR_INVALID_ARG;
-    if (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC &&
-        (!o.workspace || o.workspace_bytes < h3qk_workspace_bytes()))
-        return H3QK_ERR_INVALID_ARG;
-
     if (stride % 8) return H3QK_ERR_MISALIGNED;
     if (!aligned(qkv, 16) || !aligned(norm_wq, 16) || !aligned(norm_wk, 16)) return H3QK_ERR_MISALIGNED;
-    if (!aligned(out_q, 16) || !aligned(out_k, 16) || !aligned(out_v, 16)) return H3QK_ERR_MISALIGNED;
     if (positions && !aligned(positions, 4)) return H3QK_ERR_MISALIGNED;
-    if (e4m3 && !aligned(out_scales, 4)) return H3QK_ERR_MISALIGNED;
-    if (e4m3 && scale_mode == H3QK_SCALE_STATIC && !aligned(o.static_scales, 4)) return H3QK_ERR_MISALIGNED;
-    if (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC && !aligned(o.workspace, 16)) return H3QK_ERR_MISALIGNED;
 
-    // ---- aliasing: outputs never overlap inputs or each other ---------------
-    const int64_t esz = e4m3 ? 1 : 2;
-    const Range outs[4] = {range_of(out_q, tokens * HD * esz), range_of(out_k, tokens * HD * esz),
-                           range_of(out_v, tokens * HD * esz),
-                           range_of(out_scales, e4m3 ? 12 : 0)};
-    const Range ins[6] = {
-        range_of(qkv, tokens > 0 ? ((tokens - 1) * stride + 3 * HD) * 2 : 0),
-        range_of(norm_wq, head_dim * 4), range_of(norm_wk, head_dim * 4),
-        range_of(positions, positions ? tokens * o.n_axes * 4 : 0),
-        range_of(o.static_scales, (e4m3 && scale_mode == H3QK_SCALE_STATIC) ? 12 : 0),
-        range_of(o.workspace, (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC) ? 16 : 0)};
-    for (int i = 0; i < 4; ++i) {
-        for (int k = i + 1; k < 4; ++k)
-            if (overlap(outs[i], outs[k])) return H3QK_ERR_ALIAS;
-        for (int k = 0; k < 6; ++k)
-            if (overlap(outs[i], ins[k])) return H3QK_ERR_ALIAS;
-    }
+    plan->ins[0] = range_of(qkv, tokens > 0 ? ((tokens - 1) * stride + 3 * HD) * 2 : 0);
+    plan->ins[1] = range_of(norm_wq, head_dim * 4);
+    plan->ins[2] = range_of(norm_wk, head_dim * 4);
+    plan->ins[3] = range_of(positions, positions ? tokens * o.n_axes * 4 : 0);
+    plan->HD = HD;
 
-    // ---- launch parameters ---------------------------------------------------
-    h3qk::Params p;
+    h3qk::Params& p = plan->p;
     std::memset(&p, 0, sizeof(p));
     p.qkv = static_cast<const uint16_t*>(qkv);
     p.wq = norm_wq;
     p.wk = norm_wk;
     p.pos = positions;
-    p.out[0] = out_q;
-    p.out[1] = out_k;
-    p.out[2] = out_v;
-    p.out_scales = out_scales;
-    p.amax_words = static_cast<unsigned int*>(o.workspace);
-    p.scale_words = scale_mode == H3QK_SCALE_DYNAMIC
-                        ? p.amax_words
-                        : reinterpret_cast<const unsigned int*>(o.static_scales);
     p.rows = tokens;
     p.seq = S;
     p.valid_len = valid_len;
@@ -256,7 +229,6 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
     p.rotary_dim = rotary_dim;
     p.n_axes = o.n_axes;
     p.chunks = head_dim / 8;
-    p.dynamic = scale_mode == H3QK_SCALE_DYNAMIC ? 1 : 0;
     p.eps = o.eps;
     p.inv_d = (head_dim & (head_dim - 1)) == 0 ? 1.0f / static_cast<float>(head_dim) : 0.0f;
     // Rotary inverse frequencies theta^(-2i/d_a), in double, rounded once.
@@ -268,32 +240,170 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
             p.axis[pair] = static_cast<uint8_t>(a);
         }
 
-    const int P = next_pow2(head_dim / 8);
-    const int lpr = P < h3qk::kChunksPerLane ? 1 : P / h3qk::kChunksPerLane;
+    plan->P = next_pow2(head_dim / 8);
+    const int lpr = plan->P <= h3qk::kChunksPerLane ? 1 : plan->P / h3qk::kChunksPerLane;
     const int64_t tpw = 32 / lpr;
     const int64_t groups = (tokens + tpw - 1) / tpw;
     const int64_t want = (groups + h3qk::kWarpsPerBlock - 1) / h3qk::kWarpsPerBlock;
     const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
-    const int blocks = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const bool bf16 = in_dtype == H3QK_BF16;
-    cudaError_t e;
+    plan->blocks = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
+    plan->st = reinterpret_cast<cudaStream_t>(stream);
+    plan->bf16 = in_dtype == H3QK_BF16;
+    return H3QK_OK;
+}
 
+// True when range r overlaps any input of the plan.
+bool overlaps_inputs(const Plan& pl, Range r)
+{
+    for (int k = 0; k < 4; ++k)
+        if (overlap(r, pl.ins[k])) return true;
+    return false;
+}
+
+// Zero the amax words, then run the amax pass (skipped when no row is valid).
+h3qk_status run_amax(const Plan& pl)
+{
+    h3qk::amax_init_kernel<<<1, 32, 0, pl.st>>>(pl.p.amax_words);
+    ++g_launches;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (pl.p.rows > 0 && pl.p.valid_len > 0) {
+        e = launch(pl.bf16, pl.P, h3qk::kAmax, pl.p, pl.blocks, pl.st);
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    return H3QK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* norm_wk,
+                         const int32_t* positions, int64_t tokens, int32_t heads,
+                         int32_t head_dim, int32_t rotary_dim, int64_t valid_len,
+                         h3qk_dtype out_dtype, h3qk_scale_mode scale_mode, void* out_q,
+                         void* out_k, void* out_v, float* out_scales, const h3qk_opts* opts,
+                         h3qk_stream_t stream)
+{
+    h3qk_opts o;
+    h3qk_opts_init(&o);
+    if (opts) o = *opts;
+    const bool e4m3 = out_dtype == H3QK_E4M3;
+    Plan pl;
+    h3qk_status s = plan_inputs(qkv, norm_wq, norm_wk, positions, tokens, heads, head_dim, rotary_dim,
+                                valid_len, out_dtype == H3QK_FP16 ? H3QK_FP16 : H3QK_BF16, o, stream, &pl);
+    if (s != H3QK_OK) return s;
+    const int in_dtype = pl.bf16 ? H3QK_BF16 : H3QK_FP16;
+    if (out_dtype == H3QK_FP16 || out_dtype == H3QK_BF16) {
+        if (out_dtype != in_dtype || scale_mode != H3QK_SCALE_NONE) return H3QK_ERR_INVALID_ARG;
+    } else if (e4m3) {
+        if (scale_mode != H3QK_SCALE_DYNAMIC && scale_mode != H3QK_SCALE_STATIC) return H3QK_ERR_INVALID_ARG;
+    } else {
+        return H3QK_ERR_INVALID_ARG;
+    }
+    if (tokens > 0 && (!out_q || !out_k || !out_v)) return H3QK_ERR_INVALID_ARG;
+    if (e4m3 && !out_scales) return H3QK_ERR_INVALID_ARG;
+    if (e4m3 && scale_mode == H3QK_SCALE_STATIC && !o.static_scales) return H3QK_ERR_INVALID_ARG;
+    if (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC &&
+        (!o.workspace || o.workspace_bytes < h3qk_workspace_bytes()))
+        return H3QK_ERR_INVALID_ARG;
+    if (!aligned(out_q, 16) || !aligned(out_k, 16) || !aligned(out_v, 16)) return H3QK_ERR_MISALIGNED;
+    if (e4m3 && !aligned(out_scales, 4)) return H3QK_ERR_MISALIGNED;
+    if (e4m3 && scale_mode == H3QK_SCALE_STATIC && !aligned(o.static_scales, 4)) return H3QK_ERR_MISALIGNED;
+    if (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC && !aligned(o.workspace, 16)) return H3QK_ERR_MISALIGNED;
+
+    // Aliasing: outputs never overlap inputs or each other.
+    const int64_t esz = e4m3 ? 1 : 2;
+    const int64_t n_out = tokens * pl.HD * esz;
+    const Range outs[4] = {range_of(out_q, n_out), range_of(out_k, n_out), range_of(out_v, n_out),
+                           range_of(out_scales, e4m3 ? 12 : 0)};
+    const Range extra[2] = {
+        range_of(o.static_scales, (e4m3 && scale_mode == H3QK_SCALE_STATIC) ? 12 : 0),
+        range_of(o.workspace, (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC) ? 16 : 0)};
+    for (int i = 0; i < 4; ++i) {
+        for (int k = i + 1; k < 4; ++k)
+            if (overlap(outs[i], outs[k])) return H3QK_ERR_ALIAS;
+        if (overlaps_inputs(pl, outs[i]) || overlap(outs[i], extra[0]) || overlap(outs[i], extra[1]))
+            return H3QK_ERR_ALIAS;
+    }
+
+    h3qk::Params& p = pl.p;
+    p.out[0] = out_q;
+    p.out[1] = out_k;
+    p.out[2] = out_v;
+    p.out_scales = out_scales;
+    p.amax_words = static_cast<unsigned int*>(o.workspace);
+    p.scale_words = scale_mode == H3QK_SCALE_DYNAMIC
+                        ? p.amax_words
+                        : reinterpret_cast<const unsigned int*>(o.static_scales);
+    p.dynamic = scale_mode == H3QK_SCALE_DYNAMIC ? 1 : 0;
+    cudaError_t e;
     if (!e4m3) {
         if (tokens == 0 || valid_len == 0) return H3QK_OK;
-        e = launch(bf16, P, h3qk::kOut16, p, blocks, st);
+        e = launch(pl.bf16, pl.P, h3qk::kOut16, p, pl.blocks, pl.st);
         return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
     }
     if (scale_mode == H3QK_SCALE_DYNAMIC) {
-        h3qk::amax_init_kernel<<<1, 32, 0, st>>>(p.amax_words);
-        ++g_launches;
-        if ((e = cudaGetLastError()) != cudaSuccess) return fail_cuda(e);
-        if (tokens > 0 && valid_len > 0) {
-            e = launch(bf16, P, h3qk::kAmax, p, blocks, st);
-            if (e != cudaSuccess) return fail_cuda(e);
-        }
+        s = run_amax(pl);
+        if (s != H3QK_OK) return s;
     }
-    e = launch(bf16, P, h3qk::kCast, p, blocks, st);
+    e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.blocks, pl.st);
+    return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
+}
+
+h3qk_status h3qk_amax(const void* qkv, const float* norm_wq, const float* norm_wk,
+                      const int32_t* positions, int64_t tokens, int32_t heads, int32_t head_dim,
+                      int32_t rotary_dim, int64_t valid_len, float* out_amax, const h3qk_opts* opts,
+                      h3qk_stream_t stream)
+{
+    h3qk_opts o;
+    h3qk_opts_init(&o);
+    if (opts) o = *opts;
+    Plan pl;
+    h3qk_status s = plan_inputs(qkv, norm_wq, norm_wk, positions, tokens, heads, head_dim, rotary_dim,
+                                valid_len, H3QK_BF16, o, stream, &pl);
+    if (s != H3QK_OK) return s;
+    if (!out_amax) return H3QK_ERR_INVALID_ARG;
+    if (!aligned(out_amax, 4)) return H3QK_ERR_MISALIGNED;
+    if (overlaps_inputs(pl, range_of(out_amax, 12))) return H3QK_ERR_ALIAS;
+    pl.p.amax_words = reinterpret_cast<unsigned int*>(out_amax);
+    return run_amax(pl);
+}
+
+h3qk_status h3qk_cast(const void* qkv, const float* norm_wq, const float* norm_wk,
+                      const int32_t* positions, int64_t tokens, int32_t heads, int32_t head_dim,
+                      int32_t rotary_dim, int64_t valid_len, const float* amax, void* out_q,
+                      void* out_k, void* out_v, float* out_scales, const h3qk_opts* opts,
+                      h3qk_stream_t stream)
+{
+    h3qk_opts o;
+    h3qk_opts_init(&o);
+    if (opts) o = *opts;
+    Plan pl;
+    h3qk_status s = plan_inputs(qkv, norm_wq, norm_wk, positions, tokens, heads, head_dim, rotary_dim,
+                                valid_len, H3QK_BF16, o, stream, &pl);
+    if (s != H3QK_OK) return s;
+    if (!amax || !out_scales) return H3QK_ERR_INVALID_ARG;
+    if (tokens > 0 && (!out_q || !out_k || !out_v)) return H3QK_ERR_INVALID_ARG;
+    if (!aligned(amax, 4) || !aligned(out_scales, 4)) return H3QK_ERR_MISALIGNED;
+    if (!aligned(out_q, 16) || !aligned(out_k, 16) || !aligned(out_v, 16)) return H3QK_ERR_MISALIGNED;
+    const int64_t n_out = tokens * pl.HD;
+    const Range outs[4] = {range_of(out_q, n_out), range_of(out_k, n_out), range_of(out_v, n_out),
+                           range_of(out_scales, 12)};
+    const Range amax_r = range_of(amax, 12);
+    for (int i = 0; i < 4; ++i) {
+        for (int k = i + 1; k < 4; ++k)
+            if (overlap(outs[i], outs[k])) return H3QK_ERR_ALIAS;
+        if (overlaps_inputs(pl, outs[i]) || overlap(outs[i], amax_r)) return H3QK_ERR_ALIAS;
+    }
+    h3qk::Params& p = pl.p;
+    p.out[0] = out_q;
+    p.out[1] = out_k;
+    p.out[2] = out_v;
+    p.out_scales = out_scales;
+    p.scale_words = reinterpret_cast<const unsigned int*>(amax);
+    p.dynamic = 1;
+    const cudaError_t e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.blocks, pl.st);
     return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
 }
 

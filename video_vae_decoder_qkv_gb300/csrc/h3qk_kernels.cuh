@@ -34,24 +34,23 @@ constexpr int kMaxPairs = 128;       // rotary_dim <= 256
 constexpr int kWarpsPerBlock = 8;
 constexpr int kThreads = 32 * kWarpsPerBlock;
 // Tuning knobs (compile-time; the defaults are the measured best):
-// H3QK_CH chunks of 8 channels per lane, H3QK_UNROLL head rows per batch,
-// H3QK_PIPE prefetch of the next batch, H3QK_MIN_BLOCKS resident blocks per SM
-// asked of the register allocator.
+// H3QK_CH chunks of 8 channels per lane (1, 2 or 4), H3QK_UNROLL Q/K head rows
+// per batch of loads, H3QK_V_UNROLL V head rows per batch, H3QK_MIN_BLOCKS resident blocks
+// per SM asked of the register allocator.
 #ifndef H3QK_CH
-#define H3QK_CH 1
+#define H3QK_CH 2
 #endif
 #ifndef H3QK_UNROLL
 #define H3QK_UNROLL 4
 #endif
-#ifndef H3QK_PIPE
-#define H3QK_PIPE 0
+#ifndef H3QK_V_UNROLL
+#define H3QK_V_UNROLL 4
 #endif
 #ifndef H3QK_MIN_BLOCKS
 #define H3QK_MIN_BLOCKS 1
 #endif
 constexpr int kChunksPerLane = H3QK_CH;
 constexpr int kUnroll = H3QK_UNROLL;
-constexpr bool kPipe = H3QK_PIPE != 0;
 
 enum Mode : int { kOut16 = 0, kAmax = 1, kCast = 2 };
 
@@ -166,50 +165,137 @@ __device__ __forceinline__ uint4 load16(const uint16_t* p)
 }
 
 // ---------------------------------------------------------------------------
-// The kernel.  A head row's C = D/8 chunks (8 channels = 16 bytes each) sit
-// on LPR lanes, CH chunks per lane (chunks c, c+LPR, ..., LPR*CH =
-// next_pow2(C)); a warp covers TPW = 32/LPR token rows.  Each warp walks
-// groups of TPW rows (grid-stride) and, for each, the 3*H head rows
-// Q[0..H), K[0..H), V[0..H) in batches of U, optionally loading the next
-// batch before computing the current one (PIPE).  The reduction tree is the
-// same for every (LPR, CH): the first log2(CH) halving levels pair chunks
-// held by the same lane, the rest are xor shuffles.
-// MODE kOut16 writes 16-bit head-major outputs; kAmax reduces max |y| per
-// tensor; kCast writes e4m3 codes under the dynamic or static factors.
+// Packed product: two binary32 multiplies in one instruction, each rounded to
+// nearest even.  Used only where the product feeds no addition (the norm,
+// the weight and the e4m3 factor): a packed product that feeds a packed add
+// may be fused into a multiply-add by the code generator even with .rn and
+// --fmad=false, which would drop a rounding.  Products that feed additions
+// use __fmul_rn, which is never merged into a multiply-add.
 // ---------------------------------------------------------------------------
-template <int CH, int U>
-struct Batch {
-    uint4 v[U][CH];
-};
-
-template <int LPR, int CH, int U>
-__device__ __forceinline__ void load_batch(Batch<CH, U>& bt, const uint16_t* row, int j0, int H,
-                                           int D, int64_t HD, const bool (&act)[CH])
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
 {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Max of packed 16-bit magnitudes, NaN ignored (the other operand is kept).
+template <bool BF16>
+__device__ __forceinline__ uint32_t hmax2_abs(uint32_t m, uint32_t y)
+{
+    uint32_t a = y & 0x7fff7fffu;
+    uint32_t r;
+    if constexpr (BF16) {
+        __nv_bfloat162 v = __hmax2(*reinterpret_cast<__nv_bfloat162*>(&m), *reinterpret_cast<__nv_bfloat162*>(&a));
+        r = *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __hmax2(*reinterpret_cast<__half2*>(&m), *reinterpret_cast<__half2*>(&a));
+        r = *reinterpret_cast<uint32_t*>(&v);
+    }
+    return r;
+}
+
+template <bool BF16>
+__device__ __forceinline__ float hmax2_to_float(uint32_t m)
+{
+    const float2 f = widen2<BF16>(m);
+    return fmaxf(f.x, f.y);
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int i)
+{
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// ---------------------------------------------------------------------------
+// One Q or K head row as seen by one lane: its CH chunks of 8 channels in
+// `raw` (chunk q of lane c is chunk c + q*LPR of the row), the lane's weights
+// `w` (CH*8 floats, chunk by chunk), the rotary cos/sin and flags of its 4
+// pairs per chunk.  Computes the sum of squares (each chunk left to right;
+// the halving tree's levels that pair chunks of this lane, then xor shuffles
+// over LPR lanes), 1/sqrt(ss/D + eps), the weighted 16-bit norm and the
+// rotation, and returns the 16-bit words.
+// ---------------------------------------------------------------------------
+template <bool BF16, int LPR, int CH>
+__device__ __forceinline__ void qk_row(const uint4 (&raw)[CH], const float4* w, const float (&cs)[CH][4],
+                                       const float (&sn)[CH][4], const bool (&rot)[CH][4], float inv_d,
+                                       float eps, int D, uint32_t (&y)[CH][4])
+{
+    float x[CH][8];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int j = j0 + u;
-        const int part = j / H;
-        const int h = j - part * H;
-        const bool in = j < 3 * H;
+    for (int q = 0; q < CH; ++q)
 #pragma unroll
-        for (int q = 0; q < CH; ++q) {
-            bt.v[u][q] = make_uint4(0u, 0u, 0u, 0u);
-            if (in && act[q]) bt.v[u][q] = load16(row + part * HD + static_cast<int64_t>(h) * D + 8 * q * LPR);
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = widen2<BF16>(word(raw[q], i));
+            x[q][2 * i] = f.x;
+            x[q][2 * i + 1] = f.y;
+        }
+    // Sum of squares of each chunk, channels left to right.
+    float acc[CH];
+#pragma unroll
+    for (int q = 0; q < CH; ++q) {
+        acc[q] = __fmul_rn(x[q][0], x[q][0]);
+#pragma unroll
+        for (int k = 1; k < 8; ++k) acc[q] = __fadd_rn(acc[q], __fmul_rn(x[q][k], x[q][k]));
+    }
+    // Halving tree: chunk c+q*LPR pairs with chunk c+(q+o)*LPR in this lane
+    // for o = CH/2 ... 1, then xor shuffles over the LPR lanes.
+#pragma unroll
+    for (int o = CH / 2; o >= 1; o >>= 1)
+#pragma unroll
+        for (int q = 0; q < o; ++q) acc[q] = __fadd_rn(acc[q], acc[q + o]);
+    float ss = acc[0];
+#pragma unroll
+    for (int o = LPR / 2; o >= 1; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    const float ms = inv_d != 0.0f ? __fmul_rn(ss, inv_d) : __fdiv_rn(ss, static_cast<float>(D));
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+    const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+    for (int q = 0; q < CH; ++q) {
+        const float4 wa = w[2 * q], wb = w[2 * q + 1];
+        const float wq[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 a = mul2(mul2(make_float2(x[q][2 * i], x[q][2 * i + 1]), inv2),
+                                  make_float2(wq[2 * i], wq[2 * i + 1]));
+            const uint32_t n = round2<BF16>(a.x, a.y);
+            const float2 uv = widen2<BF16>(n);
+            const float ro = __fsub_rn(__fmul_rn(uv.x, cs[q][i]), __fmul_rn(uv.y, sn[q][i]));  // u c - v s
+            const float rv = __fadd_rn(__fmul_rn(uv.x, sn[q][i]), __fmul_rn(uv.y, cs[q][i]));  // u s + v c
+            y[q][i] = rot[q][i] ? round2<BF16>(ro, rv) : n;
         }
     }
 }
 
-template <bool BF16, int LPR, int CH, int U, bool PIPE, int MODE>
+// ---------------------------------------------------------------------------
+// The kernel.  A head row's C = D/8 chunks (8 channels = 16 bytes each) sit on
+// LPR lanes, CH chunks per lane: lane c owns chunks c, c + LPR, ..., with
+// LPR * CH = P = next_pow2(C).  A warp covers TPW = 32/LPR token rows.  Each
+// warp walks groups of TPW rows (grid-stride) and, for each, the H head rows
+// of Q, then of K (norm + RoPE), then of V (copied), U head rows per batch of
+// loads.  The reduction tree is the same for every (LPR, CH): the first
+// halving level (chunk c + chunk c+LPR) is in-lane, the rest are xor shuffles.
+// MODE kOut16 writes 16-bit head-major outputs; kAmax reduces max |y| per
+// tensor; kCast writes e4m3 codes under the dynamic or static factors.
+// ---------------------------------------------------------------------------
+template <bool BF16, int LPR, int CH, int U, int MODE>
 __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const __grid_constant__ Params p)
 {
+    static_assert(CH == 1 || CH == 2 || CH == 4, "1, 2 or 4 chunks per lane");
     constexpr int TPW = 32 / LPR;
+    constexpr int UV = H3QK_V_UNROLL;  // V head rows per batch (copy only)
     const int lane = threadIdx.x & 31;
     const int sub = lane / LPR;
     const int c = lane % LPR;
-    bool chunk_on[CH];
+    bool on[CH];
 #pragma unroll
-    for (int q = 0; q < CH; ++q) chunk_on[q] = c + q * LPR < p.chunks;
+    for (int q = 0; q < CH; ++q) on[q] = c + q * LPR < p.chunks;
     const int H = p.heads;
     const int D = p.head_dim;
     const int64_t HD = static_cast<int64_t>(H) * D;
@@ -241,25 +327,19 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
         }
     }
 
-    // This lane's norm weights of Q and K, 8 per chunk.
-    float wq[CH][8], wk[CH][8];
-#pragma unroll
-    for (int q = 0; q < CH; ++q) {
-        if (chunk_on[q]) {
-            const float4* q4 = reinterpret_cast<const float4*>(p.wq + 8 * (c + q * LPR));
-            const float4* k4 = reinterpret_cast<const float4*>(p.wk + 8 * (c + q * LPR));
-            const float4 a = __ldg(q4), b = __ldg(q4 + 1), e = __ldg(k4), f = __ldg(k4 + 1);
-            wq[q][0] = a.x; wq[q][1] = a.y; wq[q][2] = a.z; wq[q][3] = a.w;
-            wq[q][4] = b.x; wq[q][5] = b.y; wq[q][6] = b.z; wq[q][7] = b.w;
-            wk[q][0] = e.x; wk[q][1] = e.y; wk[q][2] = e.z; wk[q][3] = e.w;
-            wk[q][4] = f.x; wk[q][5] = f.y; wk[q][6] = f.z; wk[q][7] = f.w;
-        } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) wq[q][k] = wk[q][k] = 0.0f;
-        }
+    // Norm weights of Q and K in shared memory, laid out per lane:
+    // ws[part][c][q*8 + k] = weight of channel 8*(c + q*LPR) + k (zero past
+    // the head), so a lane reads its CH*8 weights as 2*CH float4.
+    __shared__ __align__(16) float ws[2][LPR][CH * 8];
+    for (int t = threadIdx.x; t < 2 * LPR * CH * 8; t += kThreads) {
+        const int part = t / (LPR * CH * 8), cc = (t / (CH * 8)) % LPR, q = (t / 8) % CH, k = t % 8;
+        const float* w = part == 0 ? p.wq : p.wk;
+        const int chunk = cc + q * LPR;
+        ws[part][cc][q * 8 + k] = chunk < p.chunks ? __ldg(w + 8 * chunk + k) : 0.0f;
     }
+    __syncthreads();
 
-    float amax[3] = {0.0f, 0.0f, 0.0f};
+    uint32_t am[3] = {0u, 0u, 0u};  // packed 16-bit running max of |y| per tensor
 
     for (int64_t g = warp0; g < n_groups; g += n_warps) {
         const int64_t r = g * TPW + sub;
@@ -272,133 +352,122 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
         }
         bool act[CH];
 #pragma unroll
-        for (int q = 0; q < CH; ++q) act[q] = act_row && chunk_on[q];
+        for (int q = 0; q < CH; ++q) act[q] = act_row && on[q];
 
-        // Rotary cos/sin of this lane's pairs (pair index 4*(c + q*LPR) + k).
+        // Rotary cos / sin of this lane's pairs: pair i of chunk q is global
+        // pair 4*(c + q*LPR) + i.
         float cs[CH][4], sn[CH][4];
         bool rot[CH][4];
 #pragma unroll
         for (int q = 0; q < CH; ++q)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int pair = 4 * (c + q * LPR) + k;
-                rot[q][k] = 2 * pair < p.rotary_dim;
-                cs[q][k] = 1.0f;
-                sn[q][k] = 0.0f;
-                if (rot[q][k] && act[q]) {
+            for (int i = 0; i < 4; ++i) {
+                const int pair = 4 * (c + q * LPR) + i;
+                rot[q][i] = 2 * pair < p.rotary_dim;
+                cs[q][i] = 1.0f;
+                sn[q][i] = 0.0f;
+                if (rot[q][i] && act[q]) {
                     const float pv = static_cast<float>(__ldg(p.pos + r * p.n_axes + p.axis[pair]));
-                    sincos_h3(__fmul_rn(pv, p.inv_freq[pair]), sn[q][k], cs[q][k]);
+                    sincos_h3(__fmul_rn(pv, p.inv_freq[pair]), sn[q][i], cs[q][i]);
                 }
             }
 
-        const uint16_t* row = p.qkv + r * p.row_stride + 8 * c;
+        const uint16_t* rowp = p.qkv + r * p.row_stride + 8 * c;
         const int64_t obase = (b * H * p.seq + s) * D + 8 * c;
 
-        Batch<CH, U> cur;
-        if constexpr (PIPE) load_batch<LPR, CH, U>(cur, row, 0, H, D, HD, act);
-        for (int j0 = 0; j0 < 3 * H; j0 += U) {
-            Batch<CH, U> nxt;
-            if constexpr (PIPE) {
-                if (j0 + U < 3 * H) load_batch<LPR, CH, U>(nxt, row, j0 + U, H, D, HD, act);
-            } else {
-                load_batch<LPR, CH, U>(cur, row, j0, H, D, HD, act);
-            }
+        // ---- Q and K: norm + RoPE ------------------------------------------
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int j = j0 + u;
-                if (j >= 3 * H) break;                 // warp-uniform
-                const int part = j / H;
-                const int h = j - part * H;
-                uint32_t y[CH][4];
-                if (part < 2) {
-                    float x[CH][8];
-                    float acc[CH];
+        for (int part = 0; part < 2; ++part) {
+            const uint16_t* src = rowp + part * HD;
+            for (int h0 = 0; h0 < H; h0 += U) {
+                uint4 raw[U][CH];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
 #pragma unroll
                     for (int q = 0; q < CH; ++q) {
-                        const uint32_t wv[4] = {cur.v[u][q].x, cur.v[u][q].y, cur.v[u][q].z, cur.v[u][q].w};
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float2 f = widen2<BF16>(wv[k]);
-                            x[q][2 * k] = f.x;
-                            x[q][2 * k + 1] = f.y;
-                        }
-                        // Sum of squares of one chunk: 8 channels left to right.
-                        acc[q] = __fmul_rn(x[q][0], x[q][0]);
-#pragma unroll
-                        for (int k = 1; k < 8; ++k) acc[q] = __fadd_rn(acc[q], __fmul_rn(x[q][k], x[q][k]));
+                        raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
+                        if (h0 + u < H && act[q])
+                            raw[u][q] = load16(src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR);
                     }
-                    // Halving tree: levels pairing chunks of this lane, then shuffles.
 #pragma unroll
-                    for (int o = CH / 2; o >= 1; o >>= 1)
+                for (int u = 0; u < U; ++u) {
+                    const int h = h0 + u;
+                    if (h >= H) break;  // warp-uniform
+                    uint4 rw[CH];
 #pragma unroll
-                        for (int q = 0; q < o; ++q) acc[q] = __fadd_rn(acc[q], acc[q + o]);
-                    float ss = acc[0];
+                    for (int q = 0; q < CH; ++q) rw[q] = raw[u][q];
+                    uint32_t y[CH][4];
+                    qk_row<BF16, LPR, CH>(rw, reinterpret_cast<const float4*>(&ws[part][c][0]), cs, sn, rot,
+                                          p.inv_d, p.eps, D, y);
 #pragma unroll
-                    for (int o = LPR / 2; o >= 1; o >>= 1)
-                        ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-                    const float ms = p.inv_d != 0.0f ? __fmul_rn(ss, p.inv_d)
-                                                     : __fdiv_rn(ss, static_cast<float>(D));
-                    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, p.eps)));
+                    for (int q = 0; q < CH; ++q) {
+                        if (!act[q]) continue;
+                        const int64_t off = obase + h * head_stride + 8 * q * LPR;
+                        if constexpr (MODE == kOut16) {
+                            uint16_t* dst = static_cast<uint16_t*>(p.out[part]) + off;
+                            *reinterpret_cast<uint4*>(dst) = make_uint4(y[q][0], y[q][1], y[q][2], y[q][3]);
+                        } else if constexpr (MODE == kAmax) {
 #pragma unroll
-                    for (int q = 0; q < CH; ++q)
+                            for (int i = 0; i < 4; ++i) am[part] = hmax2_abs<BF16>(am[part], y[q][i]);
+                        } else {
+                            const float2 fa = make_float2(fac[part], fac[part]);
+                            uint32_t cw[2];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float w0 = part == 0 ? wq[q][2 * k] : wk[q][2 * k];
-                            const float w1 = part == 0 ? wq[q][2 * k + 1] : wk[q][2 * k + 1];
-                            const float a0 = __fmul_rn(__fmul_rn(x[q][2 * k], inv), w0);
-                            const float a1 = __fmul_rn(__fmul_rn(x[q][2 * k + 1], inv), w1);
-                            uint32_t n2 = round2<BF16>(a0, a1);
-                            if (rot[q][k]) {
-                                const float2 uv = widen2<BF16>(n2);
-                                const float ro = __fsub_rn(__fmul_rn(uv.x, cs[q][k]), __fmul_rn(uv.y, sn[q][k]));
-                                const float rv = __fadd_rn(__fmul_rn(uv.x, sn[q][k]), __fmul_rn(uv.y, cs[q][k]));
-                                n2 = round2<BF16>(ro, rv);
+                            for (int i = 0; i < 2; ++i) {
+                                const float2 z0 = mul2(widen2<BF16>(y[q][2 * i]), fa);
+                                const float2 z1 = mul2(widen2<BF16>(y[q][2 * i + 1]), fa);
+                                cw[i] = e4m3x2(z0.x, z0.y) | (e4m3x2(z1.x, z1.y) << 16);
                             }
-                            y[q][k] = n2;
+                            uint8_t* dst = static_cast<uint8_t*>(p.out[part]) + off;
+                            *reinterpret_cast<uint2*>(dst) = make_uint2(cw[0], cw[1]);
                         }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < CH; ++q) {
-                        y[q][0] = cur.v[u][q].x;
-                        y[q][1] = cur.v[u][q].y;
-                        y[q][2] = cur.v[u][q].z;
-                        y[q][3] = cur.v[u][q].w;
-                    }
-                }
-
-#pragma unroll
-                for (int q = 0; q < CH; ++q) {
-                    if (!act[q]) continue;
-                    const int64_t off = obase + h * head_stride + 8 * q * LPR;
-                    if constexpr (MODE == kOut16) {
-                        uint16_t* dst = static_cast<uint16_t*>(p.out[part]) + off;
-                        *reinterpret_cast<uint4*>(dst) = make_uint4(y[q][0], y[q][1], y[q][2], y[q][3]);
-                    } else if constexpr (MODE == kAmax) {
-                        float m = 0.0f;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float2 f = widen2<BF16>(y[q][k]);
-                            m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-                        }
-                        if (part == 0) amax[0] = fmaxf(amax[0], m);
-                        else if (part == 1) amax[1] = fmaxf(amax[1], m);
-                        else amax[2] = fmaxf(amax[2], m);
-                    } else {
-                        const float fa = part == 0 ? fac[0] : (part == 1 ? fac[1] : fac[2]);
-                        uint32_t cw[2];
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            const float2 f0 = widen2<BF16>(y[q][2 * k]);
-                            const float2 f1 = widen2<BF16>(y[q][2 * k + 1]);
-                            cw[k] = e4m3x2(__fmul_rn(f0.x, fa), __fmul_rn(f0.y, fa)) |
-                                    (e4m3x2(__fmul_rn(f1.x, fa), __fmul_rn(f1.y, fa)) << 16);
-                        }
-                        uint8_t* dst = static_cast<uint8_t*>(p.out[part]) + off;
-                        *reinterpret_cast<uint2*>(dst) = make_uint2(cw[0], cw[1]);
                     }
                 }
             }
-            if constexpr (PIPE) cur = nxt;
+        }
+
+        // ---- V: passed through ----------------------------------------------
+        {
+            const uint16_t* src = rowp + 2 * HD;
+            for (int h0 = 0; h0 < H; h0 += UV) {
+                uint4 raw[UV][CH];
+#pragma unroll
+                for (int u = 0; u < UV; ++u)
+#pragma unroll
+                    for (int q = 0; q < CH; ++q) {
+                        raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
+                        if (h0 + u < H && act[q])
+                            raw[u][q] = load16(src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR);
+                    }
+#pragma unroll
+                for (int u = 0; u < UV; ++u) {
+                    const int h = h0 + u;
+                    if (h >= H) break;  // warp-uniform
+#pragma unroll
+                    for (int q = 0; q < CH; ++q) {
+                        if (!act[q]) continue;
+                        const int64_t off = obase + h * head_stride + 8 * q * LPR;
+                        if constexpr (MODE == kOut16) {
+                            uint16_t* dst = static_cast<uint16_t*>(p.out[2]) + off;
+                            *reinterpret_cast<uint4*>(dst) = raw[u][q];
+                        } else if constexpr (MODE == kAmax) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) am[2] = hmax2_abs<BF16>(am[2], word(raw[u][q], i));
+                        } else {
+                            const float2 fa = make_float2(fac[2], fac[2]);
+                            uint32_t cw[2];
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                const float2 z0 = mul2(widen2<BF16>(word(raw[u][q], 2 * i)), fa);
+                                const float2 z1 = mul2(widen2<BF16>(word(raw[u][q], 2 * i + 1)), fa);
+                                cw[i] = e4m3x2(z0.x, z0.y) | (e4m3x2(z1.x, z1.y) << 16);
+                            }
+                            uint8_t* dst = static_cast<uint8_t*>(p.out[2]) + off;
+                            *reinterpret_cast<uint2*>(dst) = make_uint2(cw[0], cw[1]);
+                        }
+                    }
+                }
+            }
         }
     }
 
@@ -406,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
         __shared__ float red[3][kWarpsPerBlock];
 #pragma unroll
         for (int t = 0; t < 3; ++t) {
-            float m = amax[t];
+            float m = hmax2_to_float<BF16>(am[t]);
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
             if (lane == 0) red[t][threadIdx.x >> 5] = m;

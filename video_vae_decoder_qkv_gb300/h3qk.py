@@ -202,3 +202,112 @@ def prepare(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rota
     if st != OK:
         raise H3QKError(st, status_string(st), int(lib().h3qk_last_cuda_error()))
     return q, k, v, (out_scales if out_dt == E4M3 else None)
+
+
+def _opts_for(qkv, *, n_axes, axis_dims, theta, eps, batch):
+    import torch
+
+    o = default_opts()
+    o.in_dtype = FP16 if qkv.dtype == torch.float16 else BF16
+    o.n_axes = n_axes
+    if axis_dims is not None:
+        dims = list(axis_dims) + [0] * (3 - len(axis_dims))
+        o.axis_dims = (ctypes.c_int32 * 3)(*dims)
+    o.eps = eps
+    o.batch = batch
+    o.qkv_row_stride = qkv.stride(0)
+    o.theta = theta
+    return o
+
+
+def _split_sigs(L):
+    P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    if L.h3qk_amax.argtypes is None:
+        L.h3qk_amax.restype = ctypes.c_int
+        L.h3qk_amax.argtypes = [P, P, P, P, I64, I32, I32, I32, I64, P, ctypes.POINTER(Opts), P]
+        L.h3qk_cast.restype = ctypes.c_int
+        L.h3qk_cast.argtypes = [P, P, P, P, I64, I32, I32, I32, I64, P, P, P, P, P,
+                                ctypes.POINTER(Opts), P]
+
+
+def amax(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rotary_dim: int,
+         batch: int = 1, valid_len: int | None = None, n_axes: int | None = None, axis_dims=None,
+         theta: float = 10000.0, eps: float = 1e-6, out=None, stream=None):
+    """The amax pass alone (h3qk_amax): a float32 [3] CUDA tensor holding the
+    largest |y| of Q, K and V over the valid rows."""
+    import torch
+
+    L = lib()
+    _split_sigs(L)
+    tokens = qkv.shape[0]
+    seq = tokens // batch
+    if valid_len is None:
+        valid_len = seq
+    if n_axes is None:
+        n_axes = positions.shape[1] if positions is not None and positions.dim() == 2 else 3
+    if out is None:
+        out = torch.empty(3, dtype=torch.float32, device=qkv.device)
+    o = _opts_for(qkv, n_axes=n_axes, axis_dims=axis_dims, theta=theta, eps=eps, batch=batch)
+    if stream is None:
+        stream = torch.cuda.current_stream(qkv.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    st = int(L.h3qk_amax(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens,
+                         heads, head_dim, rotary_dim, valid_len, out.data_ptr(), ctypes.byref(o), stream))
+    if st != OK:
+        raise H3QKError(st, status_string(st), int(L.h3qk_last_cuda_error()))
+    return out
+
+
+def cast(qkv, norm_wq, norm_wk, positions, amax_t, *, heads: int, head_dim: int, rotary_dim: int,
+         batch: int = 1, valid_len: int | None = None, n_axes: int | None = None, axis_dims=None,
+         theta: float = 10000.0, eps: float = 1e-6, out=None, out_scales=None, stream=None):
+    """The cast pass alone (h3qk_cast) under dynamic scales derived from
+    ``amax_t`` (float32 [3] CUDA tensor).  Returns (q, k, v, scales)."""
+    import torch
+
+    L = lib()
+    _split_sigs(L)
+    tokens = qkv.shape[0]
+    seq = tokens // batch
+    if valid_len is None:
+        valid_len = seq
+    if n_axes is None:
+        n_axes = positions.shape[1] if positions is not None and positions.dim() == 2 else 3
+    shape = (batch, heads, seq, head_dim)
+    if out is None:
+        out = tuple(torch.empty(shape, dtype=torch.float8_e4m3fn, device=qkv.device) for _ in range(3))
+    if out_scales is None:
+        out_scales = torch.empty(3, dtype=torch.float32, device=qkv.device)
+    q, k, v = out
+    o = _opts_for(qkv, n_axes=n_axes, axis_dims=axis_dims, theta=theta, eps=eps, batch=batch)
+    if stream is None:
+        stream = torch.cuda.current_stream(qkv.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    st = int(L.h3qk_cast(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens,
+                         heads, head_dim, rotary_dim, valid_len, amax_t.data_ptr(), q.data_ptr(),
+                         k.data_ptr(), v.data_ptr(), out_scales.data_ptr(), ctypes.byref(o), stream))
+    if st != OK:
+        raise H3QKError(st, status_string(st), int(L.h3qk_last_cuda_error()))
+    return q, k, v, out_scales
+
+
+def prepare_dynamic_sharded(qkv, norm_wq, norm_wk, positions, *, group=None, amax_fn=None,
+                            cast_fn=None, **kw):
+    """Dynamic e4m3 for rows sharded over the ranks of ``group``: the amax
+    pass on this rank's rows, an all-reduce (MAX) of the three amax values
+    over the group, then the cast pass with the shared scales, so every rank
+    casts and dequantizes with the same descales.  With ``group`` None (one
+    process) it equals prepare(..., scale_mode="dynamic").  ``amax_fn`` and
+    ``cast_fn`` default to the library's passes (:func:`amax`, :func:`cast`)."""
+    amax_fn = amax_fn or amax
+    cast_fn = cast_fn or cast
+    cast_kw = {k: v for k, v in kw.items()}
+    amax_kw = {k: v for k, v in kw.items() if k not in ("out", "out_scales")}
+    a = amax_fn(qkv, norm_wq, norm_wk, positions, **amax_kw)
+    if group is not None:
+        import torch.distributed as dist
+
+        dist.all_reduce(a, op=dist.ReduceOp.MAX, group=group)
+    return cast_fn(qkv, norm_wq, norm_wk, positions, a, **cast_kw)

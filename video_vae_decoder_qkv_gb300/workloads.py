@@ -63,7 +63,7 @@ class Spec:
     theta: float = 10000.0
     outlier_frac: float = 0.0
     outlier_scale: float = 1.0
-    dist: str = "normal"               # normal | zeros | huge | tiny | unique
+    dist: str = "normal"               # normal | zeros | huge | tiny | subsq | unique
     seed: int = 0
 
     def __post_init__(self):
@@ -178,6 +178,12 @@ def generate(spec: Spec) -> Inputs:
             # large magnitudes that push the 16-bit and e4m3 ranges
             mag = 60000.0 if spec.in_dtype == FP16 else 1e18
             x = (rng.uniform(-1, 1, (n, ncols)) * mag).astype(np.float32)
+        elif spec.dist == "subsq":
+            # magnitudes whose squares are not exact in binary32 (bf16 values
+            # in [2^-80, 2^-62]; fp16 values at its smallest subnormals)
+            lo, hi = (-80.0, -62.0) if spec.in_dtype == BF16 else (-24.0, -20.0)
+            mag = np.exp2(rng.uniform(lo, hi, (n, ncols)))
+            x = (np.where(rng.random((n, ncols)) < 0.5, -mag, mag)).astype(np.float32)
         elif spec.dist == "tiny":
             # magnitudes around the 16-bit subnormal range
             lo = 2.0 ** -24 if spec.in_dtype == FP16 else 2.0 ** -133
