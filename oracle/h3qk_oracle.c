@@ -388,6 +388,23 @@ static void h3o_problem_inv_freq(const h3o_problem* pb, float* inv_freq)
     }
 }
 
+/* Norm and rotation of one Q or K head row: D 16-bit codes in, D out.
+ * Rotated pairs use the token's cos/sin lists; channels >= R pass through
+ * normalised but unrotated. */
+static void h3o_head16(const h3o_problem* pb, const uint16_t* src, const float* w, const float* cs,
+                       const float* sn, uint16_t* dst)
+{
+    const int D = pb->head_dim, R = pb->rotary_dim;
+    float x[256];
+    uint16_t n[256];
+    for (int d = 0; d < D; ++d) x[d] = h3o_widen(pb->in_dtype, src[d]);
+    h3o_norm_head(pb->in_dtype, x, w, D, pb->eps, n);
+    for (int i = 0; i < R / 2; ++i)
+        h3o_rotate_pair(pb->in_dtype, cs[i], sn[i], n[2 * i], n[2 * i + 1],
+                        &dst[2 * i], &dst[2 * i + 1]);
+    for (int d = R; d < D; ++d) dst[d] = n[d];
+}
+
 /* ------------------------------------------------------------------------ */
 /* One packed QKV row -> the 16-bit Q, K and V values of every head.        */
 /* ------------------------------------------------------------------------ */
@@ -403,28 +420,18 @@ static void h3o_row16_with(const h3o_problem* pb, const uint16_t* qkv, const flo
                            const float* wk, const int32_t* pos, const float* inv_freq, int64_t r,
                            uint16_t* yq, uint16_t* yk, uint16_t* yv)
 {
-    const int H = pb->heads, D = pb->head_dim, R = pb->rotary_dim;
+    const int H = pb->heads, D = pb->head_dim;
     const int64_t HD = (int64_t)H * D;
     const uint16_t* row = qkv + r * pb->row_stride;
     float cs[H3O_MAX_PAIRS], sn[H3O_MAX_PAIRS];
-    float x[256];
-    uint16_t n[256];
 
     h3o_token_angles(pb, pos + r * pb->n_axes, inv_freq, cs, sn);
 
     for (int part = 0; part < 2; ++part) {
         const float* w = part == 0 ? wq : wk;
         uint16_t* y = part == 0 ? yq : yk;
-        for (int h = 0; h < H; ++h) {
-            const uint16_t* src = row + part * HD + (int64_t)h * D;
-            for (int d = 0; d < D; ++d) x[d] = h3o_widen(pb->in_dtype, src[d]);
-            h3o_norm_head(pb->in_dtype, x, w, D, pb->eps, n);
-            uint16_t* dst = y + (int64_t)h * D;
-            for (int i = 0; i < R / 2; ++i)
-                h3o_rotate_pair(pb->in_dtype, cs[i], sn[i], n[2 * i], n[2 * i + 1],
-                                &dst[2 * i], &dst[2 * i + 1]);
-            for (int d = R; d < D; ++d) dst[d] = n[d];
-        }
+        for (int h = 0; h < H; ++h)
+            h3o_head16(pb, row + part * HD + (int64_t)h * D, w, cs, sn, y + (int64_t)h * D);
     }
     const uint16_t* vsrc = row + 2 * HD;
     for (int64_t e = 0; e < HD; ++e) yv[e] = vsrc[e];
@@ -629,25 +636,16 @@ void h3o_prepare(const h3o_problem* pb, const uint16_t* qkv, const float* wq, co
 void h3o_tensor_row16(const h3o_problem* pb, int kind, const uint16_t* x, const float* w,
                       const int32_t* pos, int64_t r, uint16_t* y)
 {
-    const int H = pb->heads, D = pb->head_dim, R = pb->rotary_dim;
+    const int H = pb->heads, D = pb->head_dim;
     const uint16_t* row = x + r * pb->row_stride;
     if (kind == 2) {
         for (int64_t e = 0; e < (int64_t)H * D; ++e) y[e] = row[e];
         return;
     }
-    float inv_freq[H3O_MAX_PAIRS], cs[H3O_MAX_PAIRS], sn[H3O_MAX_PAIRS], xf[256];
-    uint16_t n[256];
+    float inv_freq[H3O_MAX_PAIRS], cs[H3O_MAX_PAIRS], sn[H3O_MAX_PAIRS];
     h3o_problem_inv_freq(pb, inv_freq);
     h3o_token_angles(pb, pos + r * pb->n_axes, inv_freq, cs, sn);
-    for (int h = 0; h < H; ++h) {
-        const uint16_t* src = row + (int64_t)h * D;
-        for (int d = 0; d < D; ++d) xf[d] = h3o_widen(pb->in_dtype, src[d]);
-        h3o_norm_head(pb->in_dtype, xf, w, D, pb->eps, n);
-        uint16_t* dst = y + (int64_t)h * D;
-        for (int i = 0; i < R / 2; ++i)
-            h3o_rotate_pair(pb->in_dtype, cs[i], sn[i], n[2 * i], n[2 * i + 1], &dst[2 * i], &dst[2 * i + 1]);
-        for (int d = R; d < D; ++d) dst[d] = n[d];
-    }
+    for (int h = 0; h < H; ++h) h3o_head16(pb, row + (int64_t)h * D, w, cs, sn, y + (int64_t)h * D);
 }
 
 /* 16-bit output of the valid rows in [row0, row1), token-major. */

@@ -40,9 +40,9 @@ MUTANTS = [
     ("rotation sign", [("*u_out = h3o_round16(dtype, uc - vs);", "*u_out = h3o_round16(dtype, uc + vs);")]),
     ("rotation operand", [("float us = u * s;", "float us = v * s;")]),
     ("half-split pairs", [("h3o_rotate_pair(pb->in_dtype, cs[i], sn[i], n[2 * i], n[2 * i + 1],\n"
-                           "                                &dst[2 * i], &dst[2 * i + 1]);",
+                           "                        &dst[2 * i], &dst[2 * i + 1]);",
                            "h3o_rotate_pair(pb->in_dtype, cs[i], sn[i], n[i], n[i + R / 2],\n"
-                           "                                &dst[i], &dst[i + R / 2]);")]),
+                           "                        &dst[i], &dst[i + R / 2]);")]),
     ("every axis uses the t position", [("float p = (float)tok_pos[a];", "float p = (float)tok_pos[0];")]),
     ("frequency exponent i/d", [("double expo = -(2.0 * (double)i) / (double)d;",
                                  "double expo = -(1.0 * (double)i) / (double)d;")]),
