@@ -254,6 +254,44 @@ def run_reference(args):
 # the CUDA path
 # --------------------------------------------------------------------------
 
+def adjacent_ops(dev, stream, iters: int = 20):
+    """The decoder block's two streaming neighbours of the path, timed after
+    the main region at 8x the B300 table's shapes (inputs above L2): SwiGLU on
+    [14376, 2 x 8192] fp16 and the scaled residual on [28752, 2048]."""
+    import torch
+
+    from video_vae_decoder_qkv_gb300 import scaled_residual, silu_and_mul
+
+    g = torch.Generator(device=dev).manual_seed(0)
+    x = torch.randn((14376, 16384), generator=g, device=dev).to(torch.float16)
+    y = torch.empty((14376, 8192), dtype=torch.float16, device=dev)
+    res = torch.randn((28752, 2048), generator=g, device=dev)
+    br = torch.randn((28752, 2048), generator=g, device=dev).to(torch.float16)
+    sc = torch.rand(2048, generator=g, device=dev)
+    out = torch.empty_like(res)
+    rows = {}
+    for name, fn, nbytes in (
+            ("silu_and_mul", lambda: silu_and_mul(x, out=y, stream=stream), x.numel() * 2 + y.numel() * 2),
+            ("scaled_residual", lambda: scaled_residual(res, br, sc, out=out, stream=stream),
+             res.numel() * 4 + br.numel() * 2 + out.numel() * 4)):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(iters):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = a.elapsed_time(b) / iters
+        rows[name] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9, "bytes": nbytes}
+    rows["silu_and_mul"]["shape"] = [14376, 16384]
+    rows["scaled_residual"]["shape"] = [28752, 2048]
+    del x, y, res, br, sc, out
+    torch.cuda.empty_cache()
+    return rows
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -365,6 +403,8 @@ def run_ours(args):
     e2e_s = es.elapsed_time(ee) / 1e3
     e2e_max, e2e_bytes = reduce_max_sum(dist, e2e_s, step_bytes * E, dev)
 
+    extra = adjacent_ops(dev, stream) if not args.tokens else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.tokens:
         rows = 16384
@@ -404,6 +444,7 @@ def run_ours(args):
             "e2e": {"value": e2e_bytes / e2e_max / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": E},
             "gpu_launches": launches,
+            "adjacent_ops": extra,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

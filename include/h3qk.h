@@ -105,7 +105,27 @@ typedef struct h3qk_opts {
                                 DYNAMIC; holds the amax words of one call, so
                                 calls that may overlap need their own */
     size_t workspace_bytes;  /* size of workspace */
+    int32_t out_layout;      /* h3qk_layout of out_q/out_k/out_v: HEAD_MAJOR
+                                [B, H, S, D] (default) or TOKEN_MAJOR [B, S, H, D] */
+    const int32_t* valid_lens; /* device int32[batch] or NULL: item b keeps rows
+                                  s < valid_lens[b] (clamped to [0, S]) instead of
+                                  valid_len (which must still lie in [0, S]) */
+    uint32_t* sat_counts;    /* device uint32[3] or NULL; e4m3 casts ADD to
+                                sat_counts[t] the number of tensor t's values
+                                whose scaled magnitude exceeds 448 (clipped to
+                                the largest code).  The caller zeroes them. */
 } h3qk_opts;
+
+typedef enum h3qk_layout {
+    H3QK_LAYOUT_HEAD_MAJOR = 0,  /* [B, H, S, D] */
+    H3QK_LAYOUT_TOKEN_MAJOR = 1  /* [B, S, H, D] */
+} h3qk_layout;
+
+typedef enum h3qk_tensor_kind {
+    H3QK_TENSOR_Q = 0, /* norm (with its weight) + RoPE */
+    H3QK_TENSOR_K = 1, /* norm (with its weight) + RoPE */
+    H3QK_TENSOR_V = 2  /* passed through */
+} h3qk_tensor_kind;
 
 /* Fill *opts with the defaults listed above. */
 void h3qk_opts_init(h3qk_opts* opts);
@@ -138,10 +158,10 @@ size_t h3qk_workspace_bytes(void);
  *              neither read for the amax nor written.
  *   out_dtype  H3QK_FP16 / H3QK_BF16 (must equal the input type) with
  *              scale_mode NONE, or H3QK_E4M3 with DYNAMIC or STATIC.
- *   out_q, out_k, out_v  [B, H, S, D] contiguous, 2 bytes (16-bit) or 1 byte
- *              (e4m3) per element; 16-byte aligned; pairwise disjoint and
- *              disjoint from every input.  Rows past valid_len keep their
- *              previous bytes.
+ *   out_q, out_k, out_v  [B, H, S, D] (or [B, S, H, D], opts->out_layout)
+ *              contiguous, 2 bytes (16-bit) or 1 byte (e4m3) per element;
+ *              16-byte aligned; pairwise disjoint and disjoint from every
+ *              input.  Rows past valid_len keep their previous bytes.
  *   out_scales float[3] descales (q, k, v) written in e4m3 modes (NULL
  *              allowed with scale_mode NONE); never the static table itself.
  *   opts       NULL or see h3qk_opts.
@@ -160,6 +180,26 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
                          h3qk_dtype out_dtype, h3qk_scale_mode scale_mode, void* out_q,
                          void* out_k, void* out_v, float* out_scales, const h3qk_opts* opts,
                          h3qk_stream_t stream);
+
+/*
+ * h3qk_norm_rope_tensor: the same path for one separately projected tensor
+ * [B, S, H, D] (rows of H*D values, row stride opts->qkv_row_stride or H*D):
+ * per-head RMS norm with norm_w and the partial RoPE for kind Q or K, the
+ * identity for kind V (norm_w may then be NULL); 16-bit output (the input
+ * type) or e4m3 with the tensor's own descale (out_scale, float[1]; dynamic
+ * from its amax over the valid rows, using opts->workspace; static from
+ * opts->static_scales[0]).  The output keeps the input's token-major
+ * [B, S, H, D] layout (opts->out_layout is ignored).  This is the
+ * single-tensor form of the pages' fused cast for the path that projects Q,
+ * K and V separately (TensorRT-LLM PR #21485, commit adding
+ * norm_rope_tensor(x, norm_weight, cos, sin, eps, fp8=...)).  Errors and
+ * asynchrony as for h3qk_prepare.
+ */
+h3qk_status h3qk_norm_rope_tensor(const void* x, const float* norm_w, const int32_t* positions,
+                                  int64_t tokens, int32_t heads, int32_t head_dim,
+                                  int32_t rotary_dim, int64_t valid_len, h3qk_tensor_kind kind,
+                                  h3qk_dtype out_dtype, h3qk_scale_mode scale_mode, void* out,
+                                  float* out_scale, const h3qk_opts* opts, h3qk_stream_t stream);
 
 /*
  * h3qk_amax and h3qk_cast: the two passes of a DYNAMIC e4m3 call, separately,
@@ -229,6 +269,36 @@ h3qk_status h3qk_prepare_noalloc(const void* qkv, const float* norm_wq, const fl
                                  h3qk_dtype out_dtype, h3qk_scale_mode scale_mode, void* out_q,
                                  void* out_k, void* out_v, float* out_scales,
                                  const h3qk_opts* opts, h3qk_stream_t stream);
+
+/*
+ * Adjacent operations of the MiniMax-H3 VAE decoder block (vllm-omni PR #6607,
+ * "Operations" table, rows "SwiGLU" and "Scaled residual"): streaming,
+ * HBM-bound, bit-exact to the test-suite's CPU oracle.
+ *
+ * h3qk_silu_and_mul: x is [rows, row_stride] 16-bit (dtype FP16 or BF16)
+ * holding gate = x[:, 0:f] and up = x[:, f:2f] (row_stride 0 means 2f; a
+ * multiple of 8); out is [rows, f] of the same type:
+ *   out = round16(silu(gate) * up),  silu(g) = g / (1 + e^-g),
+ * with a rounded sum, a correctly rounded division, a rounded product, and
+ * the library's own e^x (Cody-Waite reduction + Taylor series; the same
+ * routine as the oracle).  f is a multiple of 8; x and out 16-byte aligned
+ * and disjoint.
+ *
+ * h3qk_scaled_residual: out[r, c] = residual[r, c] + branch[r, c] * scale[c]
+ * (scale_len == channels) or * scale[0] (scale_len == 1); residual, out and
+ * scale are FP32, branch 16-bit (branch_dtype); the product is rounded on its
+ * own, then the sum ("contraction disabled").  channels is a multiple of 8;
+ * residual, branch, out (and a vector scale) 16-byte aligned; out may be
+ * residual itself (in place) but must not otherwise overlap an input.
+ *
+ * Errors and asynchrony as for h3qk_prepare.
+ */
+h3qk_status h3qk_silu_and_mul(const void* x, h3qk_dtype dtype, int64_t rows, int32_t f, int64_t row_stride,
+                              void* out, h3qk_stream_t stream);
+
+h3qk_status h3qk_scaled_residual(const float* residual, const void* branch, h3qk_dtype branch_dtype,
+                                 const float* scale, int64_t rows, int32_t channels, int32_t scale_len,
+                                 float* out, h3qk_stream_t stream);
 
 /* A static, human-readable name of a status. */
 const char* h3qk_status_string(h3qk_status status);

@@ -84,6 +84,9 @@ class _Problem(ctypes.Structure):
         ("eps", ctypes.c_float),
         ("static_scales", ctypes.c_float * 3),
         ("theta", ctypes.c_double),
+        ("out_layout", ctypes.c_int32),
+        ("pad_", ctypes.c_int32),
+        ("valid_lens", ctypes.c_void_p),
     ]
 
 
@@ -108,6 +111,8 @@ class Problem:
     theta: float = 10000.0
     static_scales: tuple = (1.0, 1.0, 1.0)
     tensor: bool = False   # one [B, S, H, D] tensor instead of packed QKV rows
+    out_layout: int = 0    # 0 head-major [B, H, S, D], 1 token-major [B, S, H, D]
+    valid_lens: tuple | None = None  # per-item valid lengths (clamped to [0, S])
 
     def __post_init__(self):
         if not self.axis_dims:
@@ -156,6 +161,11 @@ class Problem:
         p.eps = self.eps
         p.static_scales = (ctypes.c_float * 3)(*[float(s) for s in self.static_scales])
         p.theta = self.theta
+        p.out_layout = self.out_layout
+        if self.valid_lens is not None:
+            self._vl = np.ascontiguousarray(self.valid_lens, np.int32)
+            assert self._vl.shape == (self.batch,)
+            p.valid_lens = self._vl.ctypes.data
         return p
 
 
@@ -198,6 +208,12 @@ def lib():
                 "h3o_cast_row": (None, [PP, _P, _P, _P, _P, _I64, _P, _P, _P, _P]),
                 "h3o_prepare": (None, [PP, _P, _P, _P, _P, _P, _P, _P, _P]),
                 "h3o_angles_array": (None, [PP, _P, _I64, _P]),
+                "h3o_sat_rows": (None, [PP, _P, _P, _P, _P, _I64, _I64, _P, _P]),
+                "h3o_exp": (ctypes.c_float, [ctypes.c_float]),
+                "h3o_silu": (ctypes.c_float, [ctypes.c_float]),
+                "h3o_exp_array": (None, [_P, _P, _I64]),
+                "h3o_silu_and_mul_rows": (None, [ctypes.c_int, _P, _I64, ctypes.c_int, _I64, _P]),
+                "h3o_scaled_residual": (None, [ctypes.c_int, _P, _P, _P, _I64, ctypes.c_int, ctypes.c_int, _P]),
                 "h3o_tensor_row16": (None, [PP, ctypes.c_int, _P, _P, _P, _I64, _P]),
                 "h3o_tensor16_rows": (None, [PP, ctypes.c_int, _P, _P, _P, _I64, _I64, _P]),
                 "h3o_tensor_amax_rows": (ctypes.c_float, [PP, ctypes.c_int, _P, _P, _P, _I64, _I64]),
@@ -373,7 +389,8 @@ def prepare(pb: Problem, qkv, wq, wk, pos, out=None, threads: int = 1):
     (None in 16-bit mode).  Rows past valid_len keep the contents of ``out``
     (zeros when ``out`` is None)."""
     qkv, wq, wk, pos = _inputs(pb, qkv, wq, wk, pos)
-    shape = (pb.batch, pb.heads, pb.seq, pb.head_dim)
+    shape = ((pb.batch, pb.seq, pb.heads, pb.head_dim) if pb.out_layout == 1
+             else (pb.batch, pb.heads, pb.seq, pb.head_dim))
     odt = np.uint16 if pb.out_kind == OUT_16B else np.uint8
     if out is None:
         out = tuple(np.zeros(shape, odt) for _ in range(3))
@@ -460,3 +477,47 @@ def tensor_prepare(pb: Problem, kind: int, x, w, pos, out=None, threads: int = 1
         scale, factor = float(sc[k]), float(inv[k])
         list(ex.map(lambda rg: L.h3o_tensor_cast_rows(*args, rg[0], rg[1], factor, _ptr(out)), parts))
     return out, np.float32(scale)
+
+
+def sat_counts(pb: Problem, qkv, wq, wk, pos, inv) -> np.ndarray:
+    """Per-tensor counts of valid-row values whose scaled magnitude exceeds
+    448 under the factors ``inv``."""
+    qkv, wq, wk, pos = _inputs(pb, qkv, wq, wk, pos)
+    inv = _c(inv, np.float32)
+    counts = np.zeros(3, np.uint32)
+    lib().h3o_sat_rows(ctypes.byref(pb.c()), _ptr(qkv), _ptr(wq), _ptr(wk), _ptr(pos), 0, pb.rows,
+                       _ptr(inv), _ptr(counts))
+    return counts
+
+
+# --------------------------------------------------------------------------
+# Adjacent VAE-block operations (SwiGLU, scaled residual).
+# --------------------------------------------------------------------------
+
+def exp(x) -> np.ndarray:
+    x = _c(x, np.float32).reshape(-1)
+    y = np.empty_like(x)
+    lib().h3o_exp_array(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def silu_and_mul(x, f: int, dtype: int = FP16) -> np.ndarray:
+    """x: uint16 codes [rows, >= 2f] (gate | up); returns uint16 [rows, f]."""
+    x = _c(x, np.uint16)
+    rows = x.shape[0]
+    out = np.empty((rows, f), np.uint16)
+    lib().h3o_silu_and_mul_rows(dtype, _ptr(x), rows, f, x.shape[1], _ptr(out))
+    return out
+
+
+def scaled_residual(residual, branch, scale, dtype: int = FP16) -> np.ndarray:
+    """residual float32 [rows, C], branch uint16 codes [rows, C], scale
+    float32 [C] or [1]; returns float32 [rows, C]."""
+    residual = _c(residual, np.float32)
+    branch = _c(branch, np.uint16)
+    scale = _c(scale, np.float32).reshape(-1)
+    rows, C = residual.shape
+    assert branch.shape == (rows, C) and scale.size in (1, C)
+    out = np.empty_like(residual)
+    lib().h3o_scaled_residual(dtype, _ptr(residual), _ptr(branch), _ptr(scale), rows, C, scale.size, _ptr(out))
+    return out

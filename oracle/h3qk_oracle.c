@@ -69,6 +69,9 @@ typedef struct {
     float eps;            /* RMSNorm epsilon                                  */
     float static_scales[3]; /* descales for STATIC mode (q, k, v)             */
     double theta;         /* rotary base                                      */
+    int32_t out_layout;   /* 0: head-major [B, H, S, D]; 1: token-major [B, S, H, D] */
+    int32_t pad_;
+    const int32_t* valid_lens; /* per-item valid lengths (clamped to [0, S]) or NULL */
 } h3o_problem;
 
 /* ------------------------------------------------------------------------ */
@@ -447,17 +450,29 @@ void h3o_row16(const h3o_problem* pb, const uint16_t* qkv, const float* wq, cons
     h3o_row16_with(pb, qkv, wq, wk, pos, inv_freq, r, yq, yk, yv);
 }
 
+/* Row r = b*S + s is kept when s < the item's valid length: valid_lens[b]
+ * (clamped to [0, S]) when given, else valid_len [P2 valid-length commit:
+ * the per-item valid length leaves padded rows out]. */
 static int h3o_row_valid(const h3o_problem* pb, int64_t r)
 {
-    return (r % pb->seq) < pb->valid_len;
+    int64_t b = r / pb->seq, s = r % pb->seq;
+    int64_t vl = pb->valid_len;
+    if (pb->valid_lens) {
+        vl = pb->valid_lens[b];
+        if (vl < 0) vl = 0;
+        if (vl > pb->seq) vl = pb->seq;
+    }
+    return s < vl;
 }
 
 /* Offset of (row r, head h, channel 0) in a head-major [B, H, S, D] tensor
  * [P5 first commit: ggml_rope_pe_permute writes [head_dim, tokens, heads,
- * batch], innermost first]. */
+ * batch], innermost first], or in a token-major [B, S, H, D] one (the layout
+ * the cuDNN path reads [P2 norm_rope_tensor commit: [B, S, H, D]]). */
 static int64_t h3o_head_major(const h3o_problem* pb, int64_t r, int h)
 {
     int64_t b = r / pb->seq, s = r % pb->seq;
+    if (pb->out_layout == 1) return ((b * pb->seq + s) * pb->heads + h) * pb->head_dim;  /* [B, S, H, D] */
     return ((b * pb->heads + h) * pb->seq + s) * pb->head_dim;
 }
 
@@ -623,6 +638,29 @@ void h3o_prepare(const h3o_problem* pb, const uint16_t* qkv, const float* wq, co
     for (int t = 0; t < 3; ++t) out_scales[t] = scale[t];
 }
 
+/* Saturation count [P2 commit adding H3_FP8_SAT_LOG: the elements clipped at
+ * the E4M3 range, per tensor]: counts[t] += the number of valid-row values
+ * of tensor t whose scaled value y * inv[t] has magnitude above 448, the
+ * largest e4m3 code.  Reading: "clipped" means beyond the largest finite
+ * code; NaN is not counted. */
+void h3o_sat_rows(const h3o_problem* pb, const uint16_t* qkv, const float* wq, const float* wk,
+                  const int32_t* pos, int64_t row0, int64_t row1, const float* inv, uint32_t* counts)
+{
+    const int64_t HD = (int64_t)pb->heads * pb->head_dim;
+    float inv_freq[H3O_MAX_PAIRS];
+    uint16_t y[3][H3O_MAX_HD];
+    h3o_problem_inv_freq(pb, inv_freq);
+    for (int64_t r = row0; r < row1; ++r) {
+        if (!h3o_row_valid(pb, r)) continue;
+        h3o_row16_with(pb, qkv, wq, wk, pos, inv_freq, r, y[0], y[1], y[2]);
+        for (int t = 0; t < 3; ++t)
+            for (int64_t e = 0; e < HD; ++e) {
+                float z = h3o_widen(pb->in_dtype, y[t][e]) * inv[t];
+                if (fabsf(z) > 448.0f) counts[t] += 1;
+            }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Single-tensor variant [P2 norm_rope_tensor commit: one [B, S, H, D]       */
 /* tensor, norm + RoPE for Q / K, identity for V, to 16 bits or e4m3 with   */
@@ -689,6 +727,100 @@ void h3o_tensor_cast_rows(const h3o_problem* pb, int kind, const uint16_t* x, co
 }
 
 /* ------------------------------------------------------------------------ */
+/* Adjacent VAE-block operations [P3 Operations table, rows "SwiGLU" (SiLU  */
+/* and multiply after the FP16 w1 output) and "Scaled residual" (FP32       */
+/* residual + FP16 branch * FP32 scale, with contraction disabled)].        */
+/* ------------------------------------------------------------------------ */
+
+/* e^x: the library's own routine (the pages give no exp; both the CPU and
+ * the GPU evaluate this one, so SiLU agrees bit for bit).  Cody & Waite
+ * reduction x = k*ln2 + r with ln2 split in two binary32 parts (each step a
+ * fused multiply-add), the Taylor series of e^r to r^8 in Horner form, then
+ * one rounded product with 2^k (k = 128 as 2^127 then 2).  Domain handling:
+ * NaN returns NaN, x > 89 returns +inf, and results below 2^-126 (x < -87.4,
+ * where 1 + e^x already rounds to 1) return 0. */
+static const float H3O_LOG2E = 0x1.715476p+0f;
+static const float H3O_LN2_HI = 0x1.62e430p-1f;
+static const float H3O_LN2_LO = -0x1.05c610p-29f;
+static const float H3O_E2 = 0x1.000000p-1f;   /* 1/2! */
+static const float H3O_E3 = 0x1.555556p-3f;   /* 1/3! */
+static const float H3O_E4 = 0x1.555556p-5f;   /* 1/4! */
+static const float H3O_E5 = 0x1.111112p-7f;   /* 1/5! */
+static const float H3O_E6 = 0x1.6c16c2p-10f;  /* 1/6! */
+static const float H3O_E7 = 0x1.a01a02p-13f;  /* 1/7! */
+static const float H3O_E8 = 0x1.a01a02p-16f;  /* 1/8! */
+
+float h3o_exp(float x)
+{
+    if (x != x) return x;
+    if (x > 89.0f) return INFINITY;
+    if (x < -104.0f) return 0.0f;
+    float k = rintf(x * H3O_LOG2E);
+    float r = fmaf(-k, H3O_LN2_HI, x);
+    r = fmaf(-k, H3O_LN2_LO, r);
+    float p = fmaf(H3O_E8, r, H3O_E7);
+    p = fmaf(p, r, H3O_E6);
+    p = fmaf(p, r, H3O_E5);
+    p = fmaf(p, r, H3O_E4);
+    p = fmaf(p, r, H3O_E3);
+    p = fmaf(p, r, H3O_E2);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    int ki = (int)k;
+    if (ki < -126) return 0.0f;
+    /* k = 128 (x near the overflow bound): 2^128 is not a binary32, so scale
+     * by 2^127 and then by 2; both products are exact until overflow. */
+    int k1 = ki > 127 ? 127 : ki;
+    uint32_t bits = (uint32_t)(k1 + 127) << 23;
+    float two_k;
+    memcpy(&two_k, &bits, sizeof two_k);
+    float y = p * two_k;
+    if (ki > 127) y = y * 2.0f;
+    return y;
+}
+
+/* SiLU(g) = g / (1 + e^-g): one rounded sum, one correctly rounded division.
+ * Reading: the fp32 form of the reused SiluAndMul operator. */
+float h3o_silu(float g)
+{
+    float e = h3o_exp(-g);
+    float d = 1.0f + e;
+    return g / d;
+}
+
+/* SwiGLU rows: x is [rows, row_stride] 16-bit with gate = x[:, 0:f] and
+ * up = x[:, f:2f]; out[r, j] = round16(silu(gate) * up), one rounded product
+ * then the 16-bit rounding; out is [rows, f]. */
+void h3o_silu_and_mul_rows(int dtype, const uint16_t* x, int64_t rows, int f, int64_t row_stride,
+                           uint16_t* out)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int j = 0; j < f; ++j) {
+            float g = h3o_widen(dtype, x[r * row_stride + j]);
+            float u = h3o_widen(dtype, x[r * row_stride + f + j]);
+            float s = h3o_silu(g);
+            float y = s * u;
+            out[r * f + j] = h3o_round16(dtype, y);
+        }
+}
+
+/* Scaled residual: out[i] = residual[i] + branch[i] * scale[c], c = i mod
+ * channels (scale_len == channels) or 0 (scale_len == 1); the product is
+ * rounded to binary32 on its own ("contraction disabled"), then the sum. */
+void h3o_scaled_residual(int dtype, const float* residual, const uint16_t* branch, const float* scale,
+                         int64_t rows, int channels, int scale_len, float* out)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int c = 0; c < channels; ++c) {
+            int64_t i = r * channels + c;
+            float b = h3o_widen(dtype, branch[i]);
+            float sc = scale[scale_len == 1 ? 0 : c];
+            float t = b * sc;
+            out[i] = residual[i] + t;
+        }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Array helpers for the tests (element-wise loops over the scalar steps).  */
 /* ------------------------------------------------------------------------ */
 
@@ -733,4 +865,9 @@ void h3o_angles_array(const h3o_problem* pb, const int32_t* pos, int64_t n_tok, 
 void h3o_problem_inv_freq_public(const h3o_problem* pb, float* inv_freq)
 {
     h3o_problem_inv_freq(pb, inv_freq);
+}
+
+void h3o_exp_array(const float* x, float* y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = h3o_exp(x[i]);
 }

@@ -12,6 +12,7 @@ for p in (ROOT, os.path.join(ROOT, "tests")):
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libh3qk.so")
     config.addinivalue_line("markers", "slow: full-size workloads")
+    config.addinivalue_line("markers", "pure_host: touches no device memory")
 
 
 def pytest_collection_modifyitems(config, items):

@@ -298,6 +298,8 @@ def pin_hand_worked():
         elif kind == "rotate_f16":
             got = oracle.rotate_pair(case["c"], case["s"], int(case["u"], 16), int(case["v"], 16))
             assert list(got) == [int(h, 16) for h in case["expect_codes"]], (case["name"], got)
+        elif kind == "scaled_residual_f16":
+            continue  # checked by pin_scaled_residual
         elif kind == "e4m3":
             got = oracle.f32_to_e4m3(np.array(case["x"], np.float32)).tolist()
             assert got == [int(h, 16) for h in case["expect_codes"]], (case["name"], got)
@@ -630,3 +632,212 @@ def run_all() -> list[str]:
         except Exception as e:  # noqa: BLE001 - a mutant may fail in any way
             failed.append(f"{p.__name__}: {type(e).__name__}: {str(e)[:120]}")
     return failed
+
+
+# --------------------------------------------------------------------------
+# options: token-major output, per-item valid lengths, saturation counts,
+# the single-tensor variant
+# --------------------------------------------------------------------------
+
+def pin_token_major_layout():
+    """Token-major output holds, at [b, s, h, :], exactly what head-major
+    output holds at [b, h, s, :] (brute force over every element)."""
+    spec = W.TINY.with_(batch=2, seq=24, grid=(2, 3, 4), dist="unique")
+    inp = W.generate(spec)
+    hm = oracle.prepare(_problem(spec), inp.qkv, inp.wq, inp.wk, inp.pos)
+    tm = oracle.prepare(_problem(spec, out_layout=1), inp.qkv, inp.wq, inp.wk, inp.pos)
+    for a, b in zip(hm[:3], tm[:3]):
+        assert b.shape == (2, 24, 4, 64)
+        for bb in range(2):
+            for s in range(24):
+                for h in range(4):
+                    assert np.array_equal(b[bb, s, h], a[bb, h, s])
+
+
+def pin_per_item_valid_lengths():
+    """Per-item lengths (0, S, a middle value, one out of range) keep each
+    item's own prefix: canaries past it survive, rows before it equal an
+    all-valid run, and huge values past it leave the amax unchanged."""
+    spec = W.BATCHED_FP8.with_(batch=4, seq=20, grid=(1, 4, 5), in_dtype=oracle.BF16)
+    inp = W.generate(spec)
+    lens = (0, 20, 7, 99)
+    eff = (0, 20, 7, 20)
+    for kind in (0, 1):
+        pbv = _problem(spec, out_kind=kind, scale_mode=kind, valid_lens=lens)
+        pba = _problem(spec, out_kind=0, scale_mode=0)
+        odt = np.uint8 if kind else np.uint16
+        fill = 0xA5 if kind else 0x5A5A
+        shape = (4, spec.heads, 20, spec.head_dim)
+        out = tuple(np.full(shape, fill, odt) for _ in range(3))
+        got = oracle.prepare(pbv, inp.qkv, inp.wq, inp.wk, inp.pos, out=out)
+        full = oracle.prepare(pba, inp.qkv, inp.wq, inp.wk, inp.pos)
+        for t in range(3):
+            for b in range(4):
+                assert np.all(got[t][b, :, eff[b]:] == fill)
+                if kind == 0:
+                    assert np.array_equal(got[t][b, :, :eff[b]], full[t][b, :, :eff[b]])
+    pbd = _problem(spec, out_kind=1, scale_mode=1, valid_lens=lens)
+    huge = inp.qkv.copy()
+    for b in range(4):
+        huge[b * 20 + eff[b]:(b + 1) * 20] = 0x7F00
+    assert np.array_equal(oracle.amax(pbd, inp.qkv, inp.wq, inp.wk, inp.pos),
+                          oracle.amax(pbd, huge, inp.wq, inp.wk, inp.pos))
+
+
+def pin_saturation_counts():
+    """Counts equal a brute-force count (numpy) of |y * inv| > 448 over the
+    16-bit outputs; a tiny descale saturates every non-zero value, a huge one
+    none, and dynamic scales clip at most the amax element."""
+    spec = W.BATCHED_FP8.with_(batch=2, seq=40, grid=(1, 5, 8), valid_len=37)
+    inp = W.generate(spec)
+    pb16 = _problem(spec, out_kind=0, scale_mode=0)
+    y = oracle.prepare(pb16, inp.qkv, inp.wq, inp.wk, inp.pos)[:3]
+    vals = [_widen(t[:, :, :37], spec.in_dtype).astype(np.float32) for t in y]
+    pb = _problem(spec)
+    for inv in ([1.0, 1.0, 1.0], [100.0, 30.0, 200.0], [1e30, 1e30, 1e30], [1e-30, 1e-30, 1e-30]):
+        got = oracle.sat_counts(pb, inp.qkv, inp.wq, inp.wk, inp.pos, np.array(inv, np.float32))
+        want = [int(np.sum(np.abs((v * np.float32(f)).astype(np.float32)) > 448)) for v, f in zip(vals, inv)]
+        assert got.tolist() == want, (inv, got, want)
+    nz = [int(np.sum(v != 0)) for v in vals]
+    assert oracle.sat_counts(pb, inp.qkv, inp.wq, inp.wk, inp.pos, np.full(3, 1e30, np.float32)).tolist() == nz
+    # exactly +-448 is the largest code, not clipped; 450 is clipped (V passes
+    # its input through, so these values reach the cast unchanged)
+    edge = inp.qkv.copy()
+    v0 = 2 * spec.hd
+    edge[0, v0:v0 + 4] = np.array([448.0, -448.0, 450.0, 446.0], np.float32).view(np.uint32) >> 16
+    edge[1, v0:v0 + 4] = np.array([448.0, 448.0, -450.0, 0.0], np.float32).view(np.uint32) >> 16
+    one = oracle.sat_counts(pb, edge, inp.wq, inp.wk, inp.pos, np.ones(3, np.float32))
+    vv = _widen(oracle.prepare(pb16, edge, inp.wq, inp.wk, inp.pos)[2][:, :, :37], spec.in_dtype)
+    assert int(one[2]) == int(np.sum(np.abs(vv) > 448)) == 2
+    am = oracle.amax(pb, inp.qkv, inp.wq, inp.wk, inp.pos)
+    _, inv = oracle.scales(pb, am)
+    assert all(c <= 1 for c in oracle.sat_counts(pb, inp.qkv, inp.wq, inp.wk, inp.pos, inv).tolist())
+
+
+def pin_single_tensor_matches_packed():
+    """The single-tensor path on the Q (K, V) slice of packed rows gives the
+    packed path's Q (K, V) output, token-major; its e4m3 amax equals a
+    brute-force max over its 16-bit output."""
+    spec = W.DECODER_TILE.with_(batch=2, seq=30, grid=(1, 5, 6), valid_len=27, in_dtype=oracle.BF16)
+    inp = W.generate(spec)
+    HD = spec.hd
+    pbp = _problem(spec, out_layout=1)
+    packed = oracle.prepare(pbp, inp.qkv, inp.wq, inp.wk, inp.pos)
+    for kind, w in ((0, inp.wq), (1, inp.wk), (2, None)):
+        x = np.ascontiguousarray(inp.qkv[:, kind * HD:(kind + 1) * HD])
+        pbt = oracle.Problem(batch=2, seq=30, heads=spec.heads, head_dim=spec.head_dim,
+                             rotary_dim=spec.rotary_dim, in_dtype=spec.in_dtype, valid_len=27, tensor=True)
+        out, _ = oracle.tensor_prepare(pbt, kind, x, w, inp.pos)
+        assert np.array_equal(out[:, :27], packed[kind][:, :27])
+        pbd = oracle.Problem(batch=2, seq=30, heads=spec.heads, head_dim=spec.head_dim,
+                             rotary_dim=spec.rotary_dim, in_dtype=spec.in_dtype, valid_len=27, tensor=True,
+                             out_kind=1, scale_mode=1)
+        codes, scale = oracle.tensor_prepare(pbd, kind, x, w, inp.pos)
+        brute = float(np.max(np.abs(_widen(out[:, :27], spec.in_dtype))))
+        assert scale == np.float32(np.float32(brute) / np.float32(448.0))
+
+
+PINS += [pin_token_major_layout, pin_per_item_valid_lengths, pin_saturation_counts,
+         pin_single_tensor_matches_packed]
+
+
+# --------------------------------------------------------------------------
+# adjacent VAE-block operations: e^x, SiLU, SwiGLU, scaled residual
+# --------------------------------------------------------------------------
+
+def pin_exp():
+    """e^x: the constants are the binary32 roundings of log2(e), ln2 and its
+    tail, 1/n!; |e^x - libm| <= 2^-23 relative over [-17.5, 88.72] (2 M
+    points); exact at 0; e^x e^-x = 1 within 2^-22; NaN, overflow and the
+    cut-off below 2^-126."""
+    import mpmath
+
+    mpmath.mp.prec = 200
+    with open(oracle.source()) as f:
+        src = f.read()
+
+    def lit(name):
+        m = re.search(r"H3O_%s\s*=\s*(-?0x[0-9a-fA-F.]+p[-+]?\d+)f;" % name, src)
+        assert m, name
+        return float.fromhex(m.group(1))
+
+    def rn32(v):
+        with mpmath.workprec(24):
+            return float(+mpmath.mpf(v))
+
+    assert lit("LOG2E") == rn32(1 / mpmath.log(2))
+    hi = rn32(mpmath.log(2))
+    assert (lit("LN2_HI"), lit("LN2_LO")) == (hi, rn32(mpmath.log(2) - hi))
+    for n in range(2, 9):
+        assert lit("E%d" % n) == rn32(1 / mpmath.factorial(n)), n
+    x = np.linspace(-17.5, 88.72, 2_000_001).astype(np.float32)
+    y = oracle.exp(x).astype(np.float64)
+    t = np.exp(x.astype(np.float64))
+    assert np.max(np.abs(y - t) / t) <= 2.0 ** -23
+    assert oracle.lib().h3o_exp(0.0) == 1.0
+    z = np.float32(np.linspace(-17, 17, 10001))
+    assert np.max(np.abs(oracle.exp(z).astype(np.float64) * oracle.exp(-z) - 1)) <= 2.0 ** -22
+    assert np.isnan(oracle.lib().h3o_exp(float("nan")))
+    assert oracle.lib().h3o_exp(100.0) == float("inf") and oracle.lib().h3o_exp(-110.0) == 0.0
+
+
+def pin_silu():
+    """SiLU: 0 at 0; exactly g once 1 + e^-g rounds to 1 (g >= 17.4);
+    within 4 binary32 ulps of g / (1 + exp(-g)) in float64 elsewhere; the odd
+    part silu(g) - silu(-g) = g within the same bound."""
+    L = oracle.lib()
+    assert L.h3o_silu(0.0) == 0.0
+    for g in (17.5, 20.0, 1000.0, 65504.0):
+        assert L.h3o_silu(g) == np.float32(g)
+    g = np.float32(np.linspace(-30, 30, 20001))
+    got = np.array([L.h3o_silu(float(v)) for v in g], np.float64)
+    ref = g.astype(np.float64) / (1 + np.exp(-g.astype(np.float64)))
+    tol = 4 * np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64) + 1e-45
+    assert np.all(np.abs(got - ref) <= tol)
+    neg = np.array([L.h3o_silu(float(-v)) for v in g], np.float64)
+    assert np.all(np.abs((got - neg) - g) <= 8 * np.spacing(np.abs(g)).astype(np.float64) + 1e-40)
+
+
+def pin_swiglu():
+    """SwiGLU rows: gate from the first half, up from the second; every value
+    within one 16-bit ulp (plus the binary32 errors) of silu(gate) * up in
+    float64; row stride larger than 2f respected."""
+    rng = np.random.default_rng(31)
+    for dtype, to16, wid in ((oracle.FP16, oracle.f32_to_f16, _f16), (oracle.BF16, oracle.f32_to_bf16, _bf16)):
+        rows, f, stride = 7, 24, 56
+        x = to16(rng.standard_normal(rows * stride).astype(np.float32) * 3).reshape(rows, stride)
+        out = oracle.silu_and_mul(x, f, dtype)
+        g = wid(x[:, :f])
+        u = wid(x[:, f:2 * f])
+        ref = g / (1 + np.exp(-g)) * u
+        got = wid(out)
+        tol = _ulp16(ref, dtype) + 8 * 2.0 ** -24 * np.abs(ref)
+        assert np.all(np.abs(got - ref) <= tol), dtype
+
+
+def pin_scaled_residual():
+    """Power-of-two scales make the product exact, so out equals the
+    correctly rounded float64 sum; per-channel scales pick their own channel;
+    a scalar scale broadcasts; the hand-worked case shows the product's own
+    rounding (tests/golden/hand_worked.json)."""
+    rng = np.random.default_rng(32)
+    rows, C = 5, 16
+    res = rng.standard_normal((rows, C)).astype(np.float32)
+    br = oracle.f32_to_f16(rng.standard_normal(rows * C).astype(np.float32)).reshape(rows, C)
+    s = (2.0 ** rng.integers(-3, 4, C)).astype(np.float32)
+    out = oracle.scaled_residual(res, br, s, oracle.FP16)
+    exact = (res.astype(np.float64) + _f16(br) * s.astype(np.float64)).astype(np.float32)
+    assert np.array_equal(out, exact)
+    one = oracle.scaled_residual(res, br, np.array([0.5], np.float32), oracle.FP16)
+    assert np.array_equal(one, (res.astype(np.float64) + _f16(br) * 0.5).astype(np.float32))
+    with open(os.path.join(GOLDEN, "hand_worked.json")) as f:
+        cases = [c for c in json.load(f)["cases"] if c["kind"] == "scaled_residual_f16"]
+    assert cases
+    for c in cases:
+        o = oracle.scaled_residual(np.array([[c["residual"]] * 8], np.float32),
+                                   np.array([[int(c["branch"], 16)] * 8], np.uint16),
+                                   np.array([c["scale"]], np.float32), oracle.FP16)
+        assert float(o[0, 0]) == c["expect"], (c["name"], float(o[0, 0]))
+
+
+PINS += [pin_exp, pin_silu, pin_swiglu, pin_scaled_residual]

@@ -21,6 +21,20 @@ def L():
     return h3qk.lib()
 
 
+@pytest.fixture(autouse=True)
+def _fake_addresses_only_without_a_device(request):
+    """Calls below pass fake device addresses that must never reach a kernel;
+    a case that passed the host checks by mistake would launch on them.  So
+    they run only where no GPU exists (where a launch just fails)."""
+    if request.node.get_closest_marker("pure_host"):
+        return
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("fake-address ABI checks run only on hosts without a GPU")
+
+
+@pytest.mark.pure_host
 def test_every_declared_symbol_is_exported(L):
     names = h3qk.declared_functions()
     assert "h3qk_prepare" in names and len(names) >= 8
@@ -28,9 +42,11 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, n), n
 
 
+@pytest.mark.pure_host
 def test_opts_layout_and_defaults(L):
     o = h3qk.default_opts()
-    assert ctypes.sizeof(h3qk.Opts) == 72
+    assert ctypes.sizeof(h3qk.Opts) == 96
+    assert o.out_layout == 0 and not o.valid_lens and not o.sat_counts
     assert o.in_dtype == 0 and o.n_axes == 3 and list(o.axis_dims) == [0, 0, 0]
     assert o.eps == pytest.approx(1e-6, rel=1e-7) and o.batch == 1 and o.qkv_row_stride == 0
     assert o.theta == 10000.0 and not o.static_scales and not o.workspace and o.workspace_bytes == 0
@@ -38,6 +54,7 @@ def test_opts_layout_and_defaults(L):
     assert L.h3qk_version() >= 100
 
 
+@pytest.mark.pure_host
 def test_status_strings(L):
     for s in range(5):
         assert h3qk.status_string(s)
@@ -109,12 +126,7 @@ def test_aliasing_outputs(kw):
 
 def test_valid_call_without_a_device_reports_cuda_error():
     """On a host with no usable GPU a valid call gets as far as the launch and
-    reports H3QK_ERR_CUDA (a launch on a real GPU would use these fake
-    addresses, so the call is made only where no device exists)."""
-    import torch
-
-    if torch.cuda.is_available():
-        pytest.skip("a GPU is present; the fake addresses must not reach a launch")
+    reports H3QK_ERR_CUDA."""
     assert call() == h3qk.ERR_CUDA
     assert h3qk.lib().h3qk_last_cuda_error() != 0
 
@@ -149,3 +161,41 @@ def _split_call(fn, **kw):
 ])
 def test_split_entry_points_check_arguments(fn, kw, want):
     assert _split_call(fn, **kw) == want
+
+
+def _vae(fn, **kw):
+    L = h3qk.lib()
+    if fn == "silu":
+        f = L.h3qk_silu_and_mul
+        f.restype = ctypes.c_int
+        f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64,
+                      ctypes.c_void_p, ctypes.c_void_p]
+        a = dict(x=QKV, dtype=h3qk.FP16, rows=10, f=64, stride=0, out=OQ)
+        a.update(kw)
+        return f(a["x"], a["dtype"], a["rows"], a["f"], a["stride"], a["out"], None)
+    f = L.h3qk_scaled_residual
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
+                  ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    a = dict(res=OK_, br=QKV, dtype=h3qk.FP16, sc=WQ, rows=10, C=64, n_sc=64, out=OQ)
+    a.update(kw)
+    return f(a["res"], a["br"], a["dtype"], a["sc"], a["rows"], a["C"], a["n_sc"], a["out"], None)
+
+
+@pytest.mark.parametrize("fn,kw,want", [
+    ("silu", dict(f=12), h3qk.ERR_INVALID_ARG),
+    ("silu", dict(dtype=h3qk.E4M3), h3qk.ERR_INVALID_ARG),
+    ("silu", dict(stride=100), h3qk.ERR_INVALID_ARG),
+    ("silu", dict(x=None), h3qk.ERR_INVALID_ARG),
+    ("silu", dict(stride=132), h3qk.ERR_MISALIGNED),
+    ("silu", dict(out=OQ + 8), h3qk.ERR_MISALIGNED),
+    ("silu", dict(out=QKV + 256), h3qk.ERR_ALIAS),
+    ("res", dict(C=12, n_sc=12), h3qk.ERR_INVALID_ARG),
+    ("res", dict(n_sc=3), h3qk.ERR_INVALID_ARG),
+    ("res", dict(sc=None), h3qk.ERR_INVALID_ARG),
+    ("res", dict(out=OK_ + 64), h3qk.ERR_ALIAS),
+    ("res", dict(out=QKV), h3qk.ERR_ALIAS),
+    ("res", dict(res=OK_ + 4), h3qk.ERR_MISALIGNED),
+])
+def test_vae_ops_check_arguments(fn, kw, want):
+    assert _vae(fn, **kw) == want

@@ -55,15 +55,22 @@ MUTANTS = [
                              "for (int64_t e = 0; e < HD; ++e) yv[e] = vsrc[e ^ 1];")]),
     ("token-major output", [("return ((b * pb->heads + h) * pb->seq + s) * pb->head_dim;",
                              "return ((b * pb->seq + s) * pb->heads + h) * pb->head_dim;")]),
-    ("valid prefix over the whole batch", [("return (r % pb->seq) < pb->valid_len;",
-                                            "return r < pb->valid_len;")]),
+    ("valid prefix over the whole batch", [("    return s < vl;\n}", "    return r < vl;\n}")]),
+    ("per-item lengths ignored", [("        vl = pb->valid_lens[b];", "        vl = pb->valid_len;")]),
+    ("token-major head and token swapped", [
+        ("if (pb->out_layout == 1) return ((b * pb->seq + s) * pb->heads + h) * pb->head_dim;",
+         "if (pb->out_layout == 1) return ((b * pb->heads + h) * pb->seq + s) * pb->head_dim;")]),
+    ("saturation counts the largest code", [("if (fabsf(z) > 448.0f) counts[t] += 1;",
+                                             "if (fabsf(z) >= 448.0f) counts[t] += 1;")]),
     ("amax over padded rows", [("        if (!h3o_row_valid(pb, r)) continue;\n"
                                 "        h3o_row16_with(pb, qkv, wq, wk, pos, inv_freq, r, y[0], y[1], y[2]);\n"
                                 "        for (int t = 0; t < 3; ++t)\n"
-                                "            for (int64_t e = 0; e < HD; ++e) {",
+                                "            for (int64_t e = 0; e < HD; ++e) {\n"
+                                "                float a = fabsf(h3o_widen(pb->in_dtype, y[t][e]));",
                                 "        h3o_row16_with(pb, qkv, wq, wk, pos, inv_freq, r, y[0], y[1], y[2]);\n"
                                 "        for (int t = 0; t < 3; ++t)\n"
-                                "            for (int64_t e = 0; e < HD; ++e) {")]),
+                                "            for (int64_t e = 0; e < HD; ++e) {\n"
+                                "                float a = fabsf(h3o_widen(pb->in_dtype, y[t][e]));")]),
     ("descale inverted", [("s = a / 448.0f;", "s = 448.0f / a;")]),
     ("cast divides by the factor", [("float z = v * inv;", "float z = v / inv;")]),
     ("static factor not inverted", [("i = 1.0f / tab;", "i = tab;")]),
@@ -71,6 +78,14 @@ MUTANTS = [
                               "if (a > 480.0f) return (uint8_t)(sign | 0x7Eu);")]),
     ("f16 rounds half up", [("uint32_t m = (uint32_t)rintf(n);", "uint32_t m = (uint32_t)floorf(n + 0.5f);")]),
     ("bf16 subnormal exponent", [("h3o_round_sig(a, 7, -126, &E, &m);", "h3o_round_sig(a, 7, -125, &E, &m);")]),
+    ("exp reduction tail sign", [("r = fmaf(-k, H3O_LN2_LO, r);", "r = fmaf(k, H3O_LN2_LO, r);")]),
+    ("exp series one term short", [("    p = fmaf(p, r, H3O_E2);\n", "")]),
+    ("silu denominator sign", [("float d = 1.0f + e;", "float d = 1.0f - e;")]),
+    ("swiglu gate and up swapped", [("float g = h3o_widen(dtype, x[r * row_stride + j]);",
+                                     "float g = h3o_widen(dtype, x[r * row_stride + f + j]);")]),
+    ("residual fused", [("            float t = b * sc;\n            out[i] = residual[i] + t;",
+                         "            out[i] = fmaf(b, sc, residual[i]);")]),
+    ("residual scale channel", [("float sc = scale[scale_len == 1 ? 0 : c];", "float sc = scale[0];")]),
     ("f16 widening bias", [("else v = ldexpf((float)(man | 0x400), ex - 25);",
                             "else v = ldexpf((float)(man | 0x400), ex - 24);")]),
 ]

@@ -4,8 +4,12 @@ of the packed QKV projection to head-major Q/K/V, and an optional per-tensor
 e4m3 cast (dynamic or static scales, valid-prefix mask).
 
 The path is libh3qk.so (hand-written sm_103a CUDA behind the C-ABI in
-include/h3qk.h); ``prepare`` is its thin Python binding.
+include/h3qk.h); ``prepare`` is its thin Python binding.  The library also
+carries the two adjacent streaming operations of the decoder block
+(``silu_and_mul``, ``scaled_residual``).
 """
-from .h3qk import H3QKError, amax, cast, prepare, prepare_dynamic_sharded  # noqa: F401
+from .h3qk import (H3QKError, amax, cast, norm_rope_tensor, prepare,  # noqa: F401
+                   prepare_dynamic_sharded, scaled_residual, silu_and_mul)
 
-__all__ = ["prepare", "amax", "cast", "prepare_dynamic_sharded", "H3QKError"]
+__all__ = ["prepare", "norm_rope_tensor", "amax", "cast", "prepare_dynamic_sharded", "silu_and_mul",
+           "scaled_residual", "H3QKError"]

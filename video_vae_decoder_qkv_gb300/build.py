@@ -19,11 +19,12 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libh3qk.so")
-SOURCES = [os.path.join(CSRC, "h3qk_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "h3qk_kernels.cuh"), os.path.join(INCLUDE, "h3qk.h")]
+SOURCES = [os.path.join(CSRC, "h3qk_api.cu"), os.path.join(CSRC, "h3qk_vae_ops.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, "h3qk_kernels.cuh"), os.path.join(CSRC, "h3qk_internal.h"),
+                  os.path.join(INCLUDE, "h3qk.h")]
 
 NVCC_FLAGS = [
-    "-O3", "-std=c++17",
+    "-O3", "-std=c++17", "--threads", "0",
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-lineinfo",
     "-fmad=false", "-prec-div=true", "-prec-sqrt=true", "-ftz=false",

@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "h3qk.h"
+#include "h3qk_internal.h"
 #include "h3qk_kernels.cuh"
 
 namespace {
@@ -104,6 +105,10 @@ h3qk_status fail_cuda(cudaError_t e)
 
 }  // namespace
 
+int h3qk_internal_sm_count() { return sm_count(); }
+void h3qk_internal_count_launch() { ++g_launches; }
+h3qk_status h3qk_internal_fail_cuda(cudaError_t e) { return fail_cuda(e); }
+
 extern "C" {
 
 void h3qk_opts_init(h3qk_opts* o)
@@ -116,6 +121,9 @@ void h3qk_opts_init(h3qk_opts* o)
     o->batch = 1;
     o->qkv_row_stride = 0;
     o->theta = 10000.0;
+    o->out_layout = H3QK_LAYOUT_HEAD_MAJOR;
+    o->valid_lens = nullptr;
+    o->sat_counts = nullptr;
 }
 
 size_t h3qk_workspace_bytes(void) { return 16; }
@@ -152,7 +160,7 @@ struct Plan {
     int P = 1;
     int blocks = 1;
     cudaStream_t st = nullptr;
-    Range ins[4];  // qkv, norm_wq, norm_wk, positions
+    Range ins[5];  // qkv, norm_wq, norm_wk, positions, valid_lens
     int64_t HD = 0;
 };
 
@@ -162,7 +170,7 @@ struct Plan {
 h3qk_status plan_inputs(const void* qkv, const float* norm_wq, const float* norm_wk,
                         const int32_t* positions, int64_t tokens, int32_t heads, int32_t head_dim,
                         int32_t rotary_dim, int64_t valid_len, int default_in, const h3qk_opts& o,
-                        h3qk_stream_t stream, Plan* plan)
+                        h3qk_stream_t stream, Plan* plan, int parts = 3)
 {
     if (tokens < 0 || heads < 1 || heads > 65536) return H3QK_ERR_INVALID_ARG;
     if (head_dim < 8 || head_dim > 256 || head_dim % 8) return H3QK_ERR_INVALID_ARG;
@@ -193,10 +201,12 @@ h3qk_status plan_inputs(const void* qkv, const float* norm_wq, const float* norm
     if (in_dtype != H3QK_FP16 && in_dtype != H3QK_BF16) return H3QK_ERR_INVALID_ARG;
 
     const int64_t HD = static_cast<int64_t>(heads) * head_dim;
-    const int64_t stride = o.qkv_row_stride ? o.qkv_row_stride : 3 * HD;
-    if (stride < 3 * HD) return H3QK_ERR_INVALID_ARG;
+    const int64_t stride = o.qkv_row_stride ? o.qkv_row_stride : parts * HD;
+    if (stride < parts * HD) return H3QK_ERR_INVALID_ARG;
     // Byte sizes must stay far from int64 overflow.
     if (tokens > 0 && (stride > (INT64_C(1) << 40) / tokens || HD > (INT64_C(1) << 40) / tokens))
+        return H3QK_ERR_INVALID_ARG;
+    if (o.out_layout != H3QK_LAYOUT_HEAD_MAJOR && o.out_layout != H3QK_LAYOUT_TOKEN_MAJOR)
         return H3QK_ERR_INVALID_ARG;
 
     // An empty call (tokens == 0) reads and writes no row, so its row buffers
@@ -207,11 +217,14 @@ h3qk_status plan_inputs(const void* qkv, const float* norm_wq, const float* norm
     if (stride % 8) return H3QK_ERR_MISALIGNED;
     if (!aligned(qkv, 16) || !aligned(norm_wq, 16) || !aligned(norm_wk, 16)) return H3QK_ERR_MISALIGNED;
     if (positions && !aligned(positions, 4)) return H3QK_ERR_MISALIGNED;
+    if (o.valid_lens && !aligned(o.valid_lens, 4)) return H3QK_ERR_MISALIGNED;
+    if (o.sat_counts && !aligned(o.sat_counts, 4)) return H3QK_ERR_MISALIGNED;
 
-    plan->ins[0] = range_of(qkv, tokens > 0 ? ((tokens - 1) * stride + 3 * HD) * 2 : 0);
+    plan->ins[0] = range_of(qkv, tokens > 0 ? ((tokens - 1) * stride + parts * HD) * 2 : 0);
     plan->ins[1] = range_of(norm_wq, head_dim * 4);
     plan->ins[2] = range_of(norm_wk, head_dim * 4);
     plan->ins[3] = range_of(positions, positions ? tokens * o.n_axes * 4 : 0);
+    plan->ins[4] = range_of(o.valid_lens, o.valid_lens ? o.batch * 4 : 0);
     plan->HD = HD;
 
     h3qk::Params& p = plan->p;
@@ -231,6 +244,26 @@ h3qk_status plan_inputs(const void* qkv, const float* norm_wq, const float* norm
     p.chunks = head_dim / 8;
     p.eps = o.eps;
     p.inv_d = (head_dim & (head_dim - 1)) == 0 ? 1.0f / static_cast<float>(head_dim) : 0.0f;
+    // Packed rows [Q | K | V]; all three parts; one slot per part.
+    p.in_part_off[0] = 0;
+    p.in_part_off[1] = HD;
+    p.in_part_off[2] = 2 * HD;
+    p.qk_first = 0;
+    p.qk_end = 2;
+    p.has_v = 1;
+    p.slot[0] = 0;
+    p.slot[1] = 1;
+    p.slot[2] = 2;
+    p.valid_lens = o.valid_lens;
+    if (o.out_layout == H3QK_LAYOUT_TOKEN_MAJOR) {
+        p.out_bstride = S * HD;
+        p.out_sstride = HD;
+        p.out_hstride = head_dim;
+    } else {
+        p.out_bstride = static_cast<int64_t>(heads) * S * head_dim;
+        p.out_sstride = head_dim;
+        p.out_hstride = S * head_dim;
+    }
     // Rotary inverse frequencies theta^(-2i/d_a), in double, rounded once.
     int pair = 0;
     for (int a = 0; a < o.n_axes; ++a)
@@ -255,7 +288,7 @@ h3qk_status plan_inputs(const void* qkv, const float* norm_wq, const float* norm
 // True when range r overlaps any input of the plan.
 bool overlaps_inputs(const Plan& pl, Range r)
 {
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < 5; ++k)
         if (overlap(r, pl.ins[k])) return true;
     return false;
 }
@@ -267,7 +300,7 @@ h3qk_status run_amax(const Plan& pl)
     ++g_launches;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e);
-    if (pl.p.rows > 0 && pl.p.valid_len > 0) {
+    if (pl.p.rows > 0 && (pl.p.valid_len > 0 || pl.p.valid_lens)) {
         e = launch(pl.bf16, pl.P, h3qk::kAmax, pl.p, pl.blocks, pl.st);
         if (e != cudaSuccess) return fail_cuda(e);
     }
@@ -317,15 +350,18 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
     const int64_t n_out = tokens * pl.HD * esz;
     const Range outs[4] = {range_of(out_q, n_out), range_of(out_k, n_out), range_of(out_v, n_out),
                            range_of(out_scales, e4m3 ? 12 : 0)};
-    const Range extra[2] = {
+    const Range extra[3] = {
         range_of(o.static_scales, (e4m3 && scale_mode == H3QK_SCALE_STATIC) ? 12 : 0),
-        range_of(o.workspace, (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC) ? 16 : 0)};
+        range_of(o.workspace, (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC) ? 16 : 0),
+        range_of(o.sat_counts, (e4m3 && o.sat_counts) ? 12 : 0)};
     for (int i = 0; i < 4; ++i) {
         for (int k = i + 1; k < 4; ++k)
             if (overlap(outs[i], outs[k])) return H3QK_ERR_ALIAS;
-        if (overlaps_inputs(pl, outs[i]) || overlap(outs[i], extra[0]) || overlap(outs[i], extra[1]))
-            return H3QK_ERR_ALIAS;
+        if (overlaps_inputs(pl, outs[i])) return H3QK_ERR_ALIAS;
+        for (int k = 0; k < 3; ++k)
+            if (overlap(outs[i], extra[k])) return H3QK_ERR_ALIAS;
     }
+    if (e4m3 && o.sat_counts && overlaps_inputs(pl, extra[2])) return H3QK_ERR_ALIAS;
 
     h3qk::Params& p = pl.p;
     p.out[0] = out_q;
@@ -337,9 +373,10 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
                         ? p.amax_words
                         : reinterpret_cast<const unsigned int*>(o.static_scales);
     p.dynamic = scale_mode == H3QK_SCALE_DYNAMIC ? 1 : 0;
+    p.sat_counts = e4m3 ? o.sat_counts : nullptr;
     cudaError_t e;
     if (!e4m3) {
-        if (tokens == 0 || valid_len == 0) return H3QK_OK;
+        if (tokens == 0 || (valid_len == 0 && !o.valid_lens)) return H3QK_OK;
         e = launch(pl.bf16, pl.P, h3qk::kOut16, p, pl.blocks, pl.st);
         return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
     }
@@ -368,6 +405,84 @@ h3qk_status h3qk_amax(const void* qkv, const float* norm_wq, const float* norm_w
     if (overlaps_inputs(pl, range_of(out_amax, 12))) return H3QK_ERR_ALIAS;
     pl.p.amax_words = reinterpret_cast<unsigned int*>(out_amax);
     return run_amax(pl);
+}
+
+h3qk_status h3qk_norm_rope_tensor(const void* x, const float* norm_w, const int32_t* positions,
+                                  int64_t tokens, int32_t heads, int32_t head_dim,
+                                  int32_t rotary_dim, int64_t valid_len, h3qk_tensor_kind kind,
+                                  h3qk_dtype out_dtype, h3qk_scale_mode scale_mode, void* out,
+                                  float* out_scale, const h3qk_opts* opts, h3qk_stream_t stream)
+{
+    h3qk_opts o;
+    h3qk_opts_init(&o);
+    if (opts) o = *opts;
+    if (kind != H3QK_TENSOR_Q && kind != H3QK_TENSOR_K && kind != H3QK_TENSOR_V) return H3QK_ERR_INVALID_ARG;
+    // V needs no weight; its weight pointers are a stand-in that no kernel reads.
+    alignas(16) static const float kNoWeight[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const float* w = norm_w ? norm_w : (kind == H3QK_TENSOR_V ? kNoWeight : nullptr);
+    o.out_layout = H3QK_LAYOUT_TOKEN_MAJOR;
+    const bool e4m3 = out_dtype == H3QK_E4M3;
+    Plan pl;
+    h3qk_status s = plan_inputs(x, w, w, positions, tokens, heads, head_dim, rotary_dim, valid_len,
+                                out_dtype == H3QK_FP16 ? H3QK_FP16 : H3QK_BF16, o, stream, &pl, 1);
+    if (s != H3QK_OK) return s;
+    if (kind == H3QK_TENSOR_V) pl.ins[1] = pl.ins[2] = Range{0, 0};
+    const int in_dtype = pl.bf16 ? H3QK_BF16 : H3QK_FP16;
+    if (out_dtype == H3QK_FP16 || out_dtype == H3QK_BF16) {
+        if (out_dtype != in_dtype || scale_mode != H3QK_SCALE_NONE) return H3QK_ERR_INVALID_ARG;
+    } else if (e4m3) {
+        if (scale_mode != H3QK_SCALE_DYNAMIC && scale_mode != H3QK_SCALE_STATIC) return H3QK_ERR_INVALID_ARG;
+    } else {
+        return H3QK_ERR_INVALID_ARG;
+    }
+    if (tokens > 0 && !out) return H3QK_ERR_INVALID_ARG;
+    if (e4m3 && !out_scale) return H3QK_ERR_INVALID_ARG;
+    if (e4m3 && scale_mode == H3QK_SCALE_STATIC && !o.static_scales) return H3QK_ERR_INVALID_ARG;
+    if (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC &&
+        (!o.workspace || o.workspace_bytes < h3qk_workspace_bytes()))
+        return H3QK_ERR_INVALID_ARG;
+    if (!aligned(out, 16)) return H3QK_ERR_MISALIGNED;
+    if (e4m3 && !aligned(out_scale, 4)) return H3QK_ERR_MISALIGNED;
+    if (e4m3 && scale_mode == H3QK_SCALE_STATIC && !aligned(o.static_scales, 4)) return H3QK_ERR_MISALIGNED;
+    if (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC && !aligned(o.workspace, 16)) return H3QK_ERR_MISALIGNED;
+    const Range ro = range_of(out, tokens * pl.HD * (e4m3 ? 1 : 2));
+    const Range rs = range_of(out_scale, e4m3 ? 4 : 0);
+    const Range extra[3] = {
+        range_of(o.static_scales, (e4m3 && scale_mode == H3QK_SCALE_STATIC) ? 4 : 0),
+        range_of(o.workspace, (e4m3 && scale_mode == H3QK_SCALE_DYNAMIC) ? 16 : 0),
+        range_of(o.sat_counts, (e4m3 && o.sat_counts) ? 4 : 0)};
+    if (overlap(ro, rs) || overlaps_inputs(pl, ro) || overlaps_inputs(pl, rs)) return H3QK_ERR_ALIAS;
+    for (int k = 0; k < 3; ++k)
+        if (overlap(ro, extra[k]) || overlap(rs, extra[k])) return H3QK_ERR_ALIAS;
+
+    h3qk::Params& p = pl.p;
+    const int t = static_cast<int>(kind);
+    p.in_part_off[0] = p.in_part_off[1] = p.in_part_off[2] = 0;
+    p.qk_first = t < 2 ? t : 0;
+    p.qk_end = t < 2 ? t + 1 : 0;
+    p.has_v = t == 2 ? 1 : 0;
+    p.slot[0] = p.slot[1] = p.slot[2] = -1;
+    p.slot[t] = 0;
+    p.out[0] = p.out[1] = p.out[2] = out;
+    p.out_scales = out_scale;
+    p.amax_words = static_cast<unsigned int*>(o.workspace);
+    p.scale_words = scale_mode == H3QK_SCALE_DYNAMIC
+                        ? p.amax_words
+                        : reinterpret_cast<const unsigned int*>(o.static_scales);
+    p.dynamic = scale_mode == H3QK_SCALE_DYNAMIC ? 1 : 0;
+    p.sat_counts = e4m3 ? o.sat_counts : nullptr;
+    cudaError_t e;
+    if (!e4m3) {
+        if (tokens == 0 || (valid_len == 0 && !o.valid_lens)) return H3QK_OK;
+        e = launch(pl.bf16, pl.P, h3qk::kOut16, p, pl.blocks, pl.st);
+        return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
+    }
+    if (scale_mode == H3QK_SCALE_DYNAMIC) {
+        s = run_amax(pl);
+        if (s != H3QK_OK) return s;
+    }
+    e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.blocks, pl.st);
+    return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
 }
 
 h3qk_status h3qk_cast(const void* qkv, const float* norm_wq, const float* norm_wk,
@@ -403,6 +518,12 @@ h3qk_status h3qk_cast(const void* qkv, const float* norm_wq, const float* norm_w
     p.out_scales = out_scales;
     p.scale_words = reinterpret_cast<const unsigned int*>(amax);
     p.dynamic = 1;
+    if (o.sat_counts) {
+        if (overlaps_inputs(pl, range_of(o.sat_counts, 12))) return H3QK_ERR_ALIAS;
+        for (int i = 0; i < 4; ++i)
+            if (overlap(outs[i], range_of(o.sat_counts, 12))) return H3QK_ERR_ALIAS;
+        p.sat_counts = o.sat_counts;
+    }
     const cudaError_t e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.blocks, pl.st);
     return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
 }

@@ -76,6 +76,15 @@ struct Params {
     int32_t dynamic;             // cast mode: 1 dynamic, 0 static
     float eps;
     float inv_d;                 // 1/D when D is a power of two, else 0
+    int64_t in_part_off[3];      // element offset of Q, K, V within an input row
+    int64_t out_bstride;         // output element strides of item, token, head
+    int64_t out_sstride;
+    int64_t out_hstride;
+    int32_t qk_first, qk_end;    // parts [qk_first, qk_end) of {Q=0, K=1} get norm + RoPE
+    int32_t has_v;               // part 2 (V) is copied / cast
+    int32_t slot[3];             // amax / scale / count slot of each part, -1 if unused
+    const int32_t* valid_lens;   // per-item valid lengths (device), or null
+    unsigned int* sat_counts;    // cast mode: clipped-element counters (device), or null
     float inv_freq[kMaxPairs];   // per rotary pair
     uint8_t axis[kMaxPairs];     // position axis of each rotary pair
 };
@@ -273,13 +282,35 @@ __device__ __forceinline__ void qk_row(const uint4 (&raw)[CH], const float4* w, 
     }
 }
 
+// Eight 16-bit values -> eight e4m3 codes at dst (8 bytes); counts the values
+// whose scaled magnitude exceeds 448 (clipped to the largest code) into *sat.
+template <bool BF16>
+__device__ __forceinline__ void emit_e4m3(const uint32_t (&y)[4], float f, uint8_t* dst, bool count,
+                                          unsigned int& sat)
+{
+    const float2 fa = make_float2(f, f);
+    uint32_t cw[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float2 z0 = mul2(widen2<BF16>(y[2 * i]), fa);
+        const float2 z1 = mul2(widen2<BF16>(y[2 * i + 1]), fa);
+        cw[i] = e4m3x2(z0.x, z0.y) | (e4m3x2(z1.x, z1.y) << 16);
+        if (count)
+            sat += (fabsf(z0.x) > 448.0f) + (fabsf(z0.y) > 448.0f) + (fabsf(z1.x) > 448.0f) +
+                   (fabsf(z1.y) > 448.0f);
+    }
+    *reinterpret_cast<uint2*>(dst) = make_uint2(cw[0], cw[1]);
+}
+
 // ---------------------------------------------------------------------------
 // The kernel.  A head row's C = D/8 chunks (8 channels = 16 bytes each) sit on
 // LPR lanes, CH chunks per lane: lane c owns chunks c, c + LPR, ..., with
 // LPR * CH = P = next_pow2(C).  A warp covers TPW = 32/LPR token rows.  Each
 // warp walks groups of TPW rows (grid-stride) and, for each, the H head rows
 // of Q, then of K (norm + RoPE), then of V (copied), U head rows per batch of
-// loads.  The reduction tree is the same for every (LPR, CH): the first
+// loads; a call on one tensor runs only its own part.  Outputs go to
+// item * out_bstride + token * out_sstride + head * out_hstride (head-major
+// [B, H, S, D] or token-major [B, S, H, D]).  The reduction tree is the same for every (LPR, CH): the first
 // halving level (chunk c + chunk c+LPR) is in-lane, the rest are xor shuffles.
 // MODE kOut16 writes 16-bit head-major outputs; kAmax reduces max |y| per
 // tensor; kCast writes e4m3 codes under the dynamic or static factors.
@@ -298,8 +329,7 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
     for (int q = 0; q < CH; ++q) on[q] = c + q * LPR < p.chunks;
     const int H = p.heads;
     const int D = p.head_dim;
-    const int64_t HD = static_cast<int64_t>(H) * D;
-    const int64_t head_stride = p.seq * D;  // between heads of one output tensor
+    const bool count_sat = MODE == kCast && p.sat_counts != nullptr;
     const int64_t n_groups = (p.rows + TPW - 1) / TPW;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
@@ -309,8 +339,9 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
     if constexpr (MODE == kCast) {
 #pragma unroll
         for (int t = 0; t < 3; ++t) {
+            if (p.slot[t] < 0) continue;
             // One load from whichever table this mode uses (never a NULL pointer).
-            const float a = __uint_as_float(__ldcg(p.scale_words + t));
+            const float a = __uint_as_float(__ldcg(p.scale_words + p.slot[t]));
             const bool ok = a >= 1.17549435e-38f && a <= 3.40282347e+38f;
             float s = 1.0f, f = 1.0f;
             if (ok) {
@@ -323,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
                 }
             }
             fac[t] = f;
-            if (blockIdx.x == 0 && threadIdx.x == 0) p.out_scales[t] = s;
+            if (blockIdx.x == 0 && threadIdx.x == 0) p.out_scales[p.slot[t]] = s;
         }
     }
 
@@ -335,11 +366,13 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
         const int part = t / (LPR * CH * 8), cc = (t / (CH * 8)) % LPR, q = (t / 8) % CH, k = t % 8;
         const float* w = part == 0 ? p.wq : p.wk;
         const int chunk = cc + q * LPR;
-        ws[part][cc][q * 8 + k] = chunk < p.chunks ? __ldg(w + 8 * chunk + k) : 0.0f;
+        const bool used = part >= p.qk_first && part < p.qk_end;  // a V-only call has no weights
+        ws[part][cc][q * 8 + k] = used && chunk < p.chunks ? __ldg(w + 8 * chunk + k) : 0.0f;
     }
     __syncthreads();
 
     uint32_t am[3] = {0u, 0u, 0u};  // packed 16-bit running max of |y| per tensor
+    unsigned int sat[3] = {0u, 0u, 0u};
 
     for (int64_t g = warp0; g < n_groups; g += n_warps) {
         const int64_t r = g * TPW + sub;
@@ -348,7 +381,12 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
         if (r < p.rows) {
             b = r / p.seq;
             s = r - b * p.seq;
-            act_row = s < p.valid_len;
+            int64_t vl = p.valid_len;
+            if (p.valid_lens) {
+                vl = __ldg(p.valid_lens + b);
+                vl = vl < 0 ? 0 : (vl > p.seq ? p.seq : vl);
+            }
+            act_row = s < vl;
         }
         bool act[CH];
 #pragma unroll
@@ -373,12 +411,13 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
             }
 
         const uint16_t* rowp = p.qkv + r * p.row_stride + 8 * c;
-        const int64_t obase = (b * H * p.seq + s) * D + 8 * c;
+        const int64_t obase = b * p.out_bstride + s * p.out_sstride + 8 * c;
 
         // ---- Q and K: norm + RoPE ------------------------------------------
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
-            const uint16_t* src = rowp + part * HD;
+            if (part < p.qk_first || part >= p.qk_end) continue;  // warp-uniform
+            const uint16_t* src = rowp + p.in_part_off[part];
             for (int h0 = 0; h0 < H; h0 += U) {
                 uint4 raw[U][CH];
 #pragma unroll
@@ -402,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
 #pragma unroll
                     for (int q = 0; q < CH; ++q) {
                         if (!act[q]) continue;
-                        const int64_t off = obase + h * head_stride + 8 * q * LPR;
+                        const int64_t off = obase + h * p.out_hstride + 8 * q * LPR;
                         if constexpr (MODE == kOut16) {
                             uint16_t* dst = static_cast<uint16_t*>(p.out[part]) + off;
                             *reinterpret_cast<uint4*>(dst) = make_uint4(y[q][0], y[q][1], y[q][2], y[q][3]);
@@ -410,16 +449,8 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
 #pragma unroll
                             for (int i = 0; i < 4; ++i) am[part] = hmax2_abs<BF16>(am[part], y[q][i]);
                         } else {
-                            const float2 fa = make_float2(fac[part], fac[part]);
-                            uint32_t cw[2];
-#pragma unroll
-                            for (int i = 0; i < 2; ++i) {
-                                const float2 z0 = mul2(widen2<BF16>(y[q][2 * i]), fa);
-                                const float2 z1 = mul2(widen2<BF16>(y[q][2 * i + 1]), fa);
-                                cw[i] = e4m3x2(z0.x, z0.y) | (e4m3x2(z1.x, z1.y) << 16);
-                            }
-                            uint8_t* dst = static_cast<uint8_t*>(p.out[part]) + off;
-                            *reinterpret_cast<uint2*>(dst) = make_uint2(cw[0], cw[1]);
+                            emit_e4m3<BF16>(y[q], fac[part], static_cast<uint8_t*>(p.out[part]) + off, count_sat,
+                                            sat[part]);
                         }
                     }
                 }
@@ -427,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
         }
 
         // ---- V: passed through ----------------------------------------------
-        {
-            const uint16_t* src = rowp + 2 * HD;
+        if (p.has_v) {
+            const uint16_t* src = rowp + p.in_part_off[2];
             for (int h0 = 0; h0 < H; h0 += UV) {
                 uint4 raw[UV][CH];
 #pragma unroll
@@ -446,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
 #pragma unroll
                     for (int q = 0; q < CH; ++q) {
                         if (!act[q]) continue;
-                        const int64_t off = obase + h * head_stride + 8 * q * LPR;
+                        const int64_t off = obase + h * p.out_hstride + 8 * q * LPR;
                         if constexpr (MODE == kOut16) {
                             uint16_t* dst = static_cast<uint16_t*>(p.out[2]) + off;
                             *reinterpret_cast<uint4*>(dst) = raw[u][q];
@@ -454,16 +485,8 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
 #pragma unroll
                             for (int i = 0; i < 4; ++i) am[2] = hmax2_abs<BF16>(am[2], word(raw[u][q], i));
                         } else {
-                            const float2 fa = make_float2(fac[2], fac[2]);
-                            uint32_t cw[2];
-#pragma unroll
-                            for (int i = 0; i < 2; ++i) {
-                                const float2 z0 = mul2(widen2<BF16>(word(raw[u][q], 2 * i)), fa);
-                                const float2 z1 = mul2(widen2<BF16>(word(raw[u][q], 2 * i + 1)), fa);
-                                cw[i] = e4m3x2(z0.x, z0.y) | (e4m3x2(z1.x, z1.y) << 16);
-                            }
-                            uint8_t* dst = static_cast<uint8_t*>(p.out[2]) + off;
-                            *reinterpret_cast<uint2*>(dst) = make_uint2(cw[0], cw[1]);
+                            const uint32_t yv[4] = {raw[u][q].x, raw[u][q].y, raw[u][q].z, raw[u][q].w};
+                            emit_e4m3<BF16>(yv, fac[2], static_cast<uint8_t*>(p.out[2]) + off, count_sat, sat[2]);
                         }
                     }
                 }
@@ -481,12 +504,23 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
             if (lane == 0) red[t][threadIdx.x >> 5] = m;
         }
         __syncthreads();
-        if (threadIdx.x < 3) {
+        if (threadIdx.x < 3 && p.slot[threadIdx.x] >= 0) {
             float m = 0.0f;
 #pragma unroll
             for (int w = 0; w < kWarpsPerBlock; ++w) m = fmaxf(m, red[threadIdx.x][w]);
             // Non-negative binary32 values order like their bit patterns.
-            if (m > 0.0f) atomicMax(p.amax_words + threadIdx.x, __float_as_uint(m));
+            if (m > 0.0f) atomicMax(p.amax_words + p.slot[threadIdx.x], __float_as_uint(m));
+        }
+    }
+    if constexpr (MODE == kCast) {
+        if (count_sat) {
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+                unsigned int n = sat[t];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+                if (lane == 0 && n > 0 && p.slot[t] >= 0) atomicAdd(p.sat_counts + p.slot[t], n);
+            }
         }
     }
 }

@@ -18,6 +18,8 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "h3qk.h")
 DTYPE_DEFAULT, FP16, BF16, E4M3 = 0, 1, 2, 3
 SCALE_NONE, SCALE_DYNAMIC, SCALE_STATIC = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_ALIAS, ERR_CUDA = 0, 1, 2, 3, 4
+HEAD_MAJOR, TOKEN_MAJOR = 0, 1
+TENSOR_Q, TENSOR_K, TENSOR_V = 0, 1, 2
 _SCALE_NAMES = {"none": SCALE_NONE, "dynamic": SCALE_DYNAMIC, "static": SCALE_STATIC}
 
 
@@ -45,6 +47,9 @@ class Opts(ctypes.Structure):
         ("static_scales", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
+        ("out_layout", ctypes.c_int32),
+        ("valid_lens", ctypes.c_void_p),
+        ("sat_counts", ctypes.c_void_p),
     ]
 
 
@@ -138,7 +143,8 @@ def _ptr(t):
 def prepare(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rotary_dim: int,
             batch: int = 1, valid_len: int | None = None, scale_mode: str = "none",
             n_axes: int | None = None, axis_dims=None, theta: float = 10000.0, eps: float = 1e-6,
-            static_scales=None, out=None, out_scales=None, workspace=None, stream=None):
+            static_scales=None, out=None, out_scales=None, workspace=None, stream=None,
+            out_layout: str = "head_major", valid_lens=None, sat_counts=None):
     """The fused QK-prep path on torch CUDA tensors.
 
     qkv: fp16/bf16 [tokens, row_stride] (row stride a multiple of 8 elements,
@@ -149,7 +155,10 @@ def prepare(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rota
     head-major [batch, heads, S, head_dim], scales a float32 [3] tensor of
     descales in e4m3 modes, else None.  ``out``, ``out_scales`` and
     ``workspace`` reuse caller buffers (rows past valid_len of ``out`` keep
-    their contents).
+    their contents).  ``out_layout="token_major"`` writes [batch, S, heads,
+    head_dim]; ``valid_lens`` (int32 [batch] CUDA tensor) gives each item its
+    own valid length; ``sat_counts`` (int32/uint32 [3] CUDA tensor, zeroed by
+    the caller) receives the e4m3 saturation counts.
     """
     import torch
 
@@ -169,7 +178,8 @@ def prepare(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rota
     if n_axes is None:
         n_axes = positions.shape[1] if positions is not None and positions.dim() == 2 else 3
     dev = qkv.device
-    shape = (batch, heads, seq, head_dim)
+    layout = {"head_major": HEAD_MAJOR, "token_major": TOKEN_MAJOR}[out_layout]
+    shape = (batch, heads, seq, head_dim) if layout == HEAD_MAJOR else (batch, seq, heads, head_dim)
     if out is None:
         tdt = qkv.dtype if out_dt != E4M3 else torch.float8_e4m3fn
         out = tuple(torch.empty(shape, dtype=tdt, device=dev) for _ in range(3))
@@ -189,6 +199,9 @@ def prepare(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rota
     o.qkv_row_stride = qkv.stride(0)
     o.theta = theta
     o.static_scales = _ptr(static_scales)
+    o.out_layout = layout
+    o.valid_lens = _ptr(valid_lens)
+    o.sat_counts = _ptr(sat_counts)
     if workspace is not None:
         o.workspace = workspace.data_ptr()
         o.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -311,3 +324,114 @@ def prepare_dynamic_sharded(qkv, norm_wq, norm_wk, positions, *, group=None, ama
 
         dist.all_reduce(a, op=dist.ReduceOp.MAX, group=group)
     return cast_fn(qkv, norm_wq, norm_wk, positions, a, **cast_kw)
+
+
+def norm_rope_tensor(x, norm_w, positions, *, kind: str, heads: int, head_dim: int, rotary_dim: int,
+                     batch: int = 1, valid_len: int | None = None, scale_mode: str = "none",
+                     n_axes: int | None = None, axis_dims=None, theta: float = 10000.0, eps: float = 1e-6,
+                     static_scale=None, out=None, out_scale=None, workspace=None, stream=None,
+                     valid_lens=None, sat_counts=None):
+    """One separately projected tensor x [tokens, >= heads*head_dim]
+    (token-major [batch, S, heads, head_dim] rows): norm + RoPE for kind "q"
+    or "k" (``norm_w`` float32 [head_dim]), identity for "v" (``norm_w`` may
+    be None); 16-bit out (x's type) or e4m3 with its own descale.  Returns
+    (out, scale): out token-major [batch, S, heads, head_dim], scale a
+    float32 [1] tensor in e4m3 modes, else None."""
+    import torch
+
+    L = lib()
+    fn = L.h3qk_norm_rope_tensor
+    if fn.argtypes is None:
+        P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        fn.restype = ctypes.c_int
+        fn.argtypes = [P, P, P, I64, I32, I32, I32, I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
+                       ctypes.POINTER(Opts), P]
+    k = {"q": TENSOR_Q, "k": TENSOR_K, "v": TENSOR_V}[kind]
+    if x.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("x must be float16 or bfloat16")
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D [tokens, row_stride] with unit inner stride")
+    tokens = x.shape[0]
+    seq = tokens // batch
+    if valid_len is None:
+        valid_len = seq
+    mode = _SCALE_NAMES[scale_mode]
+    out_dt = (FP16 if x.dtype == torch.float16 else BF16) if mode == SCALE_NONE else E4M3
+    if n_axes is None:
+        n_axes = positions.shape[1] if positions is not None and positions.dim() == 2 else 3
+    if out is None:
+        tdt = x.dtype if out_dt != E4M3 else torch.float8_e4m3fn
+        out = torch.empty((batch, seq, heads, head_dim), dtype=tdt, device=x.device)
+    if out_dt == E4M3 and out_scale is None:
+        out_scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    if mode == SCALE_DYNAMIC and workspace is None:
+        workspace = torch.empty(int(L.h3qk_workspace_bytes()) // 4, dtype=torch.int32, device=x.device)
+    o = _opts_for(x, n_axes=n_axes, axis_dims=axis_dims, theta=theta, eps=eps, batch=batch)
+    o.static_scales = _ptr(static_scale)
+    o.valid_lens = _ptr(valid_lens)
+    o.sat_counts = _ptr(sat_counts)
+    if workspace is not None:
+        o.workspace = workspace.data_ptr()
+        o.workspace_bytes = workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    st = int(fn(x.data_ptr(), _ptr(norm_w), _ptr(positions), tokens, heads, head_dim, rotary_dim, valid_len,
+                k, out_dt, mode, out.data_ptr(), _ptr(out_scale) if out_dt == E4M3 else None,
+                ctypes.byref(o), stream))
+    if st != OK:
+        raise H3QKError(st, status_string(st), int(L.h3qk_last_cuda_error()))
+    return out, (out_scale if out_dt == E4M3 else None)
+
+
+def silu_and_mul(x, *, out=None, stream=None):
+    """SwiGLU after the w1 projection: x fp16/bf16 [rows, 2f] (gate | up,
+    row stride a multiple of 8) -> out [rows, f] = silu(gate) * up, rounded
+    as the library documents (h3qk_silu_and_mul)."""
+    import torch
+
+    L = lib()
+    fn = L.h3qk_silu_and_mul
+    if fn.argtypes is None:
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64,
+                       ctypes.c_void_p, ctypes.c_void_p]
+    if x.dtype not in (torch.float16, torch.bfloat16) or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D fp16/bf16 tensor with unit inner stride")
+    rows, two_f = x.shape
+    f = two_f // 2
+    if out is None:
+        out = torch.empty((rows, f), dtype=x.dtype, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    dt = FP16 if x.dtype == torch.float16 else BF16
+    st = int(fn(x.data_ptr(), dt, rows, f, x.stride(0), out.data_ptr(), stream))
+    if st != OK:
+        raise H3QKError(st, status_string(st), int(L.h3qk_last_cuda_error()))
+    return out
+
+
+def scaled_residual(residual, branch, scale, *, out=None, stream=None):
+    """residual float32 [rows, C] + branch fp16/bf16 [rows, C] * scale float32
+    [C] or [1], the product rounded on its own (h3qk_scaled_residual).
+    ``out=residual`` updates in place."""
+    import torch
+
+    L = lib()
+    fn = L.h3qk_scaled_residual
+    if fn.argtypes is None:
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
+                       ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    rows, C = residual.shape
+    if out is None:
+        out = torch.empty_like(residual)
+    if stream is None:
+        stream = torch.cuda.current_stream(residual.device).cuda_stream
+    dt = FP16 if branch.dtype == torch.float16 else BF16
+    st = int(fn(residual.data_ptr(), branch.data_ptr(), dt, scale.data_ptr(), rows, C, scale.numel(),
+                out.data_ptr(), stream))
+    if st != OK:
+        raise H3QKError(st, status_string(st), int(L.h3qk_last_cuda_error()))
+    return out
