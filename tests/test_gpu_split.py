@@ -71,3 +71,37 @@ def test_row_shards_with_combined_amax_equal_one_call():
         got = np.concatenate(codes[t], axis=2)
         G.assert_codes_equal(got, G.host_codes(want[t])[:, :, :spec.valid_len], f"shards {name}")
     assert np.array_equal(scales[0], scales[1]) and np.array_equal(scales[0], want[3].cpu().numpy())
+
+
+@pytest.mark.parametrize("pattern", ["late_max", "rising", "falling", "near_tie", "uniform"])
+@pytest.mark.parametrize("dtype", [W.FP16, W.BF16])
+def test_amax_early_out_is_exact(pattern, dtype):
+    """The amax pass skips rows whose bound cannot exceed the running max;
+    adversarial orders of magnitudes must still give the exact amax."""
+    import torch
+
+    spec = W.LATENT_65K.with_(name="eo", batch=2, seq=257, grid=(1, 1, 257), valid_len=250, in_dtype=dtype,
+                              out_kind=W.OUT_E4M3, scale_mode=W.SCALE_DYNAMIC)
+    inp = G.inputs(spec)
+    vals = (inp.qkv.view(np.float16).astype(np.float32) if dtype == W.FP16
+            else (inp.qkv.astype(np.uint32) << 16).view(np.float32)).copy()
+    rows = spec.rows
+    HD = spec.hd
+    if pattern == "late_max":
+        vals[1 * spec.seq + 249, 5 * 128 + 17] = 900.0          # last valid row of item 1, Q head 5
+        vals[0 * spec.seq + 249, HD + 7 * 128 + 100] = -700.0    # K, pass-through channel
+    elif pattern == "rising":
+        vals *= np.linspace(0.05, 3.0, rows, dtype=np.float32)[:, None]
+    elif pattern == "falling":
+        vals *= np.linspace(3.0, 0.05, rows, dtype=np.float32)[:, None]
+    elif pattern == "near_tie":
+        vals[:, :] = np.float32(1.0)
+        vals[137, 3 * 128 + 5] = np.float32(1.0078125)
+    conv = oracle.f32_to_f16 if dtype == W.FP16 else oracle.f32_to_bf16
+    qkv = conv(vals).reshape(inp.qkv.shape)
+    mod = W.Inputs(spec, qkv, inp.wq, inp.wk, inp.pos, inp.static_scales)
+    dev = G.to_device(mod)
+    a = h3_amax(*dev, **_kw(spec))
+    torch.cuda.synchronize()
+    ref = oracle.amax(G.problem(spec), qkv, inp.wq, inp.wk, inp.pos, threads=G.THREADS)
+    assert np.array_equal(a.cpu().numpy().view(np.uint32), ref.view(np.uint32)), (a.cpu().numpy(), ref)

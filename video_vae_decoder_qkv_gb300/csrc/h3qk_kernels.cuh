@@ -282,6 +282,40 @@ __device__ __forceinline__ void qk_row(const uint4 (&raw)[CH], const float4* w, 
     }
 }
 
+// Upper bound on |y| over one Q/K head row slice (amax pass early-out).
+// Every 16-bit output y of the row satisfies
+//   |y| <= sqrt(2) (1 + 2^-8)^2 (1 + 2^-22) max|x| max|w| inv + 2^-24
+//       <= 1.4253 max|x| max|w| inv + 2^-24:
+// a rotated pair obeys |u c - v s| <= sqrt(u^2 + v^2) sqrt(c^2 + s^2) with
+// c^2 + s^2 <= 1 + 7e-7 (the sine/cosine error bound), each of the two
+// 16-bit roundings adds at most 2^-8 relative (plus half a subnormal step),
+// the binary32 products and sums 2^-24 each.  The bound evaluates inv from an
+// approximate sum of squares (fused multiply-adds, any order) and rsqrtf,
+// within 2^-19 relative of the exact inv, and takes 1.45 and 2^-23, a margin
+// of 1.7 % over the exact bound.  max|x| comes from the packed 16-bit inputs
+// (exact), max|w| is the lane's largest weight.  A NaN or infinite input gives
+// a NaN or infinite bound, which never allows a skip.
+template <bool BF16, int LPR, int CH>
+__device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, float inv_d, float eps, int D)
+{
+    uint32_t m2 = 0u;
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int q = 0; q < CH; ++q)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w = word(raw[q], i);
+            m2 = hmax2_abs<BF16>(m2, w);
+            const float2 x = widen2<BF16>(w);
+            acc = __ffma2_rn(x, x, acc);
+        }
+    float ss = acc.x + acc.y;
+#pragma unroll
+    for (int o = LPR / 2; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = rsqrtf(ss * (inv_d != 0.0f ? inv_d : 1.0f / static_cast<float>(D)) + eps);
+    return 1.45f * inv * hmax2_to_float<BF16>(m2) * wmax + 0x1p-23f;
+}
+
 // Eight 16-bit values -> eight e4m3 codes at dst (8 bytes); counts the values
 // whose scaled magnitude exceeds 448 (clipped to the largest code) into *sat.
 template <bool BF16>
@@ -370,6 +404,16 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
         ws[part][cc][q * 8 + k] = used && chunk < p.chunks ? __ldg(w + 8 * chunk + k) : 0.0f;
     }
     __syncthreads();
+    // Largest |weight| of this lane per part (the amax pass's row bound).
+    float wmax[2] = {0.0f, 0.0f};
+    if constexpr (MODE == kAmax) {
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int k = 0; k < CH * 8; ++k) wmax[part] = fmaxf(wmax[part], fabsf(ws[part][c][k]));
+    }
+    // Warp-uniform running max of the exact |y| seen per part (binary32 bits).
+    uint32_t run[3] = {0u, 0u, 0u};
 
     uint32_t am[3] = {0u, 0u, 0u};  // packed 16-bit running max of |y| per tensor
     unsigned int sat[3] = {0u, 0u, 0u};
@@ -435,6 +479,13 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
                     uint4 rw[CH];
 #pragma unroll
                     for (int q = 0; q < CH; ++q) rw[q] = raw[u][q];
+                    if constexpr (MODE == kAmax) {
+                        // Exact early-out: when no lane's bound exceeds the largest
+                        // exact |y| this warp has seen, the row cannot raise the amax.
+                        const float bnd = qk_bound<BF16, LPR, CH>(rw, wmax[part], p.inv_d, p.eps, D);
+                        const uint32_t bb = act_row ? __float_as_uint(bnd) : 0u;
+                        if (__reduce_max_sync(0xffffffffu, bb) <= run[part]) continue;  // warp-uniform
+                    }
                     uint32_t y[CH][4];
                     qk_row<BF16, LPR, CH>(rw, reinterpret_cast<const float4*>(&ws[part][c][0]), cs, sn, rot,
                                           p.inv_d, p.eps, D, y);
@@ -453,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
                                             sat[part]);
                         }
                     }
+                    if constexpr (MODE == kAmax)
+                        run[part] = __reduce_max_sync(0xffffffffu, __float_as_uint(hmax2_to_float<BF16>(am[part])));
                 }
             }
         }
