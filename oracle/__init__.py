@@ -219,6 +219,10 @@ def lib():
                 "h3o_tensor_amax_rows": (ctypes.c_float, [PP, ctypes.c_int, _P, _P, _P, _I64, _I64]),
                 "h3o_tensor_cast_rows": (None, [PP, ctypes.c_int, _P, _P, _P, _I64, _I64, ctypes.c_float, _P]),
                 "h3o_problem_inv_freq_public": (None, [PP, _P]),
+                "h3o_norm_head_f32": (None, [_P, _P, ctypes.c_int, ctypes.c_float, _P]),
+                "h3o_rotate_f32": (None, [ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                          _P, _P]),
+                "h3o_sage_rows": (None, [PP, _P, _P, _P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(L, name)
@@ -416,6 +420,42 @@ def prepare(pb: Problem, qkv, wq, wk, pos, out=None, threads: int = 1):
         list(ex.map(lambda rg: L.h3o_cast_rows(*args, rg[0], rg[1], _ptr(inv), _ptr(q), _ptr(k), _ptr(v)),
                     parts))
     return q, k, v, sc
+
+
+def sage(pb: Problem, qkv, wq, wk, pos, kv_scale: float = 1.0, out=None, threads: int = 1):
+    """The sage-attention outputs: (q, k, v) head-major [B, H, S, D] (or
+    token-major, ``pb.out_layout``); q and k float32 (k times kv_scale), v
+    binary16 codes (uint16) of v times kv_scale.  Rows past the valid prefix
+    keep the contents of ``out`` (zeros when None)."""
+    qkv, wq, wk, pos = _inputs(pb, qkv, wq, wk, pos)
+    shape = ((pb.batch, pb.seq, pb.heads, pb.head_dim) if pb.out_layout == 1
+             else (pb.batch, pb.heads, pb.seq, pb.head_dim))
+    if out is None:
+        out = (np.zeros(shape, np.float32), np.zeros(shape, np.float32), np.zeros(shape, np.uint16))
+    q, k, v = out
+    for t, dt in zip(out, (np.float32, np.float32, np.uint16)):
+        assert t.dtype == dt and t.shape == shape and t.flags.c_contiguous
+    L, cp = lib(), pb.c()
+    args = (ctypes.byref(cp), _ptr(qkv), _ptr(wq), _ptr(wk), _ptr(pos), float(kv_scale))
+    parts = _ranges(pb.rows, max(1, threads))
+    with ThreadPoolExecutor(max(1, threads)) as ex:
+        list(ex.map(lambda rg: L.h3o_sage_rows(*args, rg[0], rg[1], _ptr(q), _ptr(k), _ptr(v)), parts))
+    return q, k, v
+
+
+def norm_head_f32(x, w, eps: float = 1e-6) -> np.ndarray:
+    x = _c(x, np.float32)
+    w = _c(w, np.float32)
+    y = np.empty(x.size, np.float32)
+    lib().h3o_norm_head_f32(_ptr(x), _ptr(w), x.size, eps, _ptr(y))
+    return y
+
+
+def rotate_f32(c: float, s: float, u: float, v: float):
+    uo = np.empty(1, np.float32)
+    vo = np.empty(1, np.float32)
+    lib().h3o_rotate_f32(float(c), float(s), float(u), float(v), _ptr(uo), _ptr(vo))
+    return uo[0], vo[0]
 
 
 def cast_rows(pb: Problem, qkv, wq, wk, pos, inv, rows):

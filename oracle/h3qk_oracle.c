@@ -323,6 +323,17 @@ float h3o_rms_inv(const float* x, int D, float eps)
     return 1.0f / rt;
 }
 
+/* Normalise one head row in binary32: y[d] = (x[d] * inv) * w[d], two
+ * rounded products in that order. */
+void h3o_norm_head_f32(const float* x, const float* w, int D, float eps, float* y)
+{
+    float inv = h3o_rms_inv(x, D, eps);
+    for (int d = 0; d < D; ++d) {
+        float xn = x[d] * inv;
+        y[d] = xn * w[d];
+    }
+}
+
 /* Normalise one head row and round it to the 16-bit type:
  * n[d] = round16((x[d] * inv) * w[d]), two rounded products in that order.
  * Reading: one rounding point after the norm, as an unfused norm kernel
@@ -330,12 +341,9 @@ float h3o_rms_inv(const float* x, int D, float eps)
  * decoder-attention commit: "normalise q/k in place on the projection"]. */
 void h3o_norm_head(int dtype, const float* x, const float* w, int D, float eps, uint16_t* n)
 {
-    float inv = h3o_rms_inv(x, D, eps);
-    for (int d = 0; d < D; ++d) {
-        float xn = x[d] * inv;
-        float y = xn * w[d];
-        n[d] = h3o_round16(dtype, y);
-    }
+    float y[256];
+    h3o_norm_head_f32(x, w, D, eps, y);
+    for (int d = 0; d < D; ++d) n[d] = h3o_round16(dtype, y[d]);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -343,20 +351,28 @@ void h3o_norm_head(int dtype, const float* x, const float* w, int D, float eps, 
 /* "partial RoPE"; P2 fused-cast commit: Q and K are rotated].              */
 /* ------------------------------------------------------------------------ */
 
+/* The rotation in binary32: (u, v) -> (u*c - v*s, u*s + v*c), every product
+ * rounded, then one rounded subtract or add (no fusion). */
+void h3o_rotate_f32(float c, float s, float u, float v, float* u_out, float* v_out)
+{
+    float uc = u * c;
+    float vs = v * s;
+    float us = u * s;
+    float vc = v * c;
+    *u_out = uc - vs;
+    *v_out = us + vc;
+}
+
 /* Rotate one pair (u, v) by the angle whose cosine and sine are (c, s):
  *   u' = round16(u*c - v*s),  v' = round16(u*s + v*c),
  * every product rounded, then one rounded add or subtract (no fusion). */
 void h3o_rotate_pair(int dtype, float c, float s, uint16_t u16, uint16_t v16,
                      uint16_t* u_out, uint16_t* v_out)
 {
-    float u = h3o_widen(dtype, u16);
-    float v = h3o_widen(dtype, v16);
-    float uc = u * c;
-    float vs = v * s;
-    float us = u * s;
-    float vc = v * c;
-    *u_out = h3o_round16(dtype, uc - vs);
-    *v_out = h3o_round16(dtype, us + vc);
+    float a, b;
+    h3o_rotate_f32(c, s, h3o_widen(dtype, u16), h3o_widen(dtype, v16), &a, &b);
+    *u_out = h3o_round16(dtype, a);
+    *v_out = h3o_round16(dtype, b);
 }
 
 /* Cosines and sines of one token's rotary angles, listed pair by pair over
@@ -723,6 +739,65 @@ void h3o_tensor_cast_rows(const h3o_problem* pb, int kind, const uint16_t* x, co
         if (!h3o_row_valid(pb, r)) continue;
         h3o_tensor_row16(pb, kind, x, w, pos, r, y);
         h3o_cast_values(pb->in_dtype, y, HD, inv, out + r * HD);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sage-attention outputs [P5 first commit: the fused RoPE / permute op     */
+/* writes head-major [head_dim, tokens, heads, batch] tensors for the sage  */
+/* kernel: F32 Q, F32 K * kv_scale and F16 V * kv_scale, with the rounding  */
+/* points of the unfused sage chain].                                       */
+/* Readings: the projection is 16-bit here (the rest of the path reads      */
+/* 16-bit rows), widened exactly; from there every step stays binary32, as  */
+/* in an all-F32 chain: the normalised value is NOT rounded to 16 bits      */
+/* before the rotation, and Q and K are written unrounded; K is scaled      */
+/* after the rotation by one rounded product with kv_scale; V is widened,   */
+/* multiplied by kv_scale (one rounded product) and rounded to binary16     */
+/* (nearest even, overflow to infinity).  No valid-prefix rule differs from */
+/* the 16-bit path.                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Norm and rotation of one Q or K head row in binary32: D 16-bit codes in,
+ * D binary32 values out; channels >= R pass through normalised. */
+static void h3o_head_f32(const h3o_problem* pb, const uint16_t* src, const float* w, const float* cs,
+                         const float* sn, float* dst)
+{
+    const int D = pb->head_dim, R = pb->rotary_dim;
+    float x[256], n[256];
+    for (int d = 0; d < D; ++d) x[d] = h3o_widen(pb->in_dtype, src[d]);
+    h3o_norm_head_f32(x, w, D, pb->eps, n);
+    for (int i = 0; i < R / 2; ++i)
+        h3o_rotate_f32(cs[i], sn[i], n[2 * i], n[2 * i + 1], &dst[2 * i], &dst[2 * i + 1]);
+    memcpy(dst + R, n + R, sizeof(float) * (size_t)(D - R));
+}
+
+/* Sage outputs of the valid rows in [row0, row1), head-major [B, H, S, D]
+ * (or token-major, pb->out_layout): out_q, out_k binary32, out_v binary16
+ * codes.  Padded rows are not written. */
+void h3o_sage_rows(const h3o_problem* pb, const uint16_t* qkv, const float* wq, const float* wk,
+                   const int32_t* pos, float kv_scale, int64_t row0, int64_t row1, float* out_q,
+                   float* out_k, uint16_t* out_v)
+{
+    const int H = pb->heads, D = pb->head_dim;
+    const int64_t HD = (int64_t)H * D;
+    float inv_freq[H3O_MAX_PAIRS], cs[H3O_MAX_PAIRS], sn[H3O_MAX_PAIRS];
+    float y[256];
+    h3o_problem_inv_freq(pb, inv_freq);
+    for (int64_t r = row0; r < row1; ++r) {
+        if (!h3o_row_valid(pb, r)) continue;
+        const uint16_t* row = qkv + r * pb->row_stride;
+        h3o_token_angles(pb, pos + r * pb->n_axes, inv_freq, cs, sn);
+        for (int h = 0; h < H; ++h) {
+            const int64_t o = h3o_head_major(pb, r, h);
+            h3o_head_f32(pb, row + (int64_t)h * D, wq, cs, sn, out_q + o);
+            h3o_head_f32(pb, row + HD + (int64_t)h * D, wk, cs, sn, y);
+            for (int d = 0; d < D; ++d) out_k[o + d] = y[d] * kv_scale;
+            const uint16_t* v = row + 2 * HD + (int64_t)h * D;
+            for (int d = 0; d < D; ++d) {
+                float sv = h3o_widen(pb->in_dtype, v[d]) * kv_scale;
+                out_v[o + d] = h3o_f32_to_f16(sv);
+            }
+        }
     }
 }
 

@@ -841,3 +841,109 @@ def pin_scaled_residual():
 
 
 PINS += [pin_exp, pin_silu, pin_swiglu, pin_scaled_residual]
+
+
+# --------------------------------------------------------------------------
+# sage-attention outputs: F32 Q, F32 K * kv_scale, F16 V * kv_scale
+# --------------------------------------------------------------------------
+
+def _sage_spec(dtype, **kw):
+    d = dict(name="sage", batch=2, seq=30, grid=(2, 3, 5), valid_len=None, in_dtype=dtype)
+    d.update(kw)
+    return W.LATENT_65K.with_(**d)
+
+
+def _head_index(pb, r, h):
+    b, s = divmod(r, pb.seq)
+    return (b, s, h) if pb.out_layout == 1 else (b, h, s)
+
+
+def pin_sage_vs_float64():
+    """Q and K of the sage outputs lie within binary32 error of the float64
+    mathematics (x / sqrt(mean x^2 + eps) * w, rotated by the binary32
+    angles; K times kv_scale): |err| <= 2^-17 (|u| + |v|) on rotated pairs
+    and 2^-17 |n| elsewhere.  A 16-bit rounding anywhere in the chain
+    (2^-11 or 2^-8 relative) or a misplaced kv_scale breaks it.  Checked at
+    every (b, h, s) of both layouts, so the placement is pinned too."""
+    for dtype in (oracle.FP16, oracle.BF16):
+        for layout in (0, 1):
+            spec = _sage_spec(dtype)
+            inp = W.generate(spec)
+            pb = _problem(spec, out_layout=layout)
+            kvs = 0.3
+            q, k, v = oracle.sage(pb, inp.qkv, inp.wq, inp.wk, inp.pos, kv_scale=kvs)
+            R = pb.rotary_dim
+            for r in range(pb.rows):
+                ((eq, _), (ek, _)), _ = _exact_path(inp, pb, r)
+                # pre-rotation magnitudes from the float64 norm
+                for got_t, e, scale in ((q, eq, 1.0), (k, ek, kvs)):
+                    for h in range(pb.heads):
+                        g = got_t[_head_index(pb, r, h)].astype(np.float64)
+                        ee = e[h] * scale
+                        mag = np.abs(ee).copy()
+                        pair = np.abs(ee[0:R:2]) + np.abs(ee[1:R:2])
+                        mag[0:R:2] = pair
+                        mag[1:R:2] = pair
+                        tol = 2.0 ** -17 * mag + 1e-30
+                        assert np.all(np.abs(g - ee) <= tol), (dtype, layout, r, h, np.max(np.abs(g - ee) / tol))
+
+
+def pin_sage_v_matches_numpy():
+    """V codes equal numpy's binary16 conversion of float32(v) *
+    float32(kv_scale) for both input types, including products that
+    overflow binary16 (to infinity) and land in its subnormal range."""
+    for dtype in (oracle.FP16, oracle.BF16):
+        spec = _sage_spec(dtype, batch=1, seq=12, grid=(1, 3, 4))
+        inp = W.generate(spec)
+        pb = _problem(spec)
+        HD = pb.hd
+        for kvs in (1.0, 0.3, 3.0e4, 1.0e-6):
+            _, _, v = oracle.sage(pb, inp.qkv, inp.wq, inp.wk, inp.pos, kv_scale=kvs)
+            for r in range(pb.rows):
+                x = _widen(inp.qkv[r, 2 * HD:3 * HD], dtype).astype(np.float32)
+                want = (x * np.float32(kvs)).astype(np.float16).view(np.uint16).reshape(pb.heads, -1)
+                for h in range(pb.heads):
+                    assert np.array_equal(v[_head_index(pb, r, h)], want[h]), (dtype, kvs, r, h)
+
+
+def pin_sage_agrees_with_16bit_path():
+    """Where the rotation is the identity (position (0, 0, 0): cos 1, sin 0)
+    or absent (rotary_dim 0), the 16-bit rounding of the sage Q and K (with
+    kv_scale 1) is the 16-bit path's output, code for code: the two differ
+    only in where the 16-bit rounding sits."""
+    for dtype in (oracle.FP16, oracle.BF16):
+        for rd in (48, 0):
+            spec = _sage_spec(dtype, rotary_dim=rd, axis_dims=(16, 16, 16) if rd else (0, 0, 0))
+            inp = W.generate(spec)
+            pos = np.zeros_like(inp.pos) if rd else inp.pos
+            pb = _problem(spec)
+            q, k, _ = oracle.sage(pb, inp.qkv, inp.wq, inp.wk, pos, kv_scale=1.0)
+            q16, k16, _, _ = oracle.prepare(pb, inp.qkv, inp.wq, inp.wk, pos)
+            conv = oracle.f32_to_f16 if dtype == oracle.FP16 else oracle.f32_to_bf16
+            for a, b in ((q, q16), (k, k16)):
+                assert np.array_equal(conv(a.reshape(-1)).reshape(a.shape), b), (dtype, rd)
+
+
+def pin_sage_kv_scale_and_prefix():
+    """A power-of-two kv_scale scales K exactly (K(2^-3) = K(1) / 8) and
+    leaves Q alone; rows past each item's valid length keep the canary."""
+    spec = _sage_spec(oracle.BF16)
+    inp = W.generate(spec)
+    pb = _problem(spec)
+    q1, k1, _ = oracle.sage(pb, inp.qkv, inp.wq, inp.wk, inp.pos, kv_scale=1.0)
+    q8, k8, _ = oracle.sage(pb, inp.qkv, inp.wq, inp.wk, inp.pos, kv_scale=0.125)
+    assert np.array_equal(q1.view(np.uint32), q8.view(np.uint32))
+    assert np.array_equal(k8, k1 / np.float32(8))
+    pbv = _problem(spec, valid_len=17)
+    shape = q1.shape
+    canary = (np.full(shape, np.float32(-7.25)), np.full(shape, np.float32(-7.25)),
+              np.full(shape, 0x5A5A, np.uint16))
+    qv, kv, vv = oracle.sage(pbv, inp.qkv, inp.wq, inp.wk, inp.pos, kv_scale=1.0, out=canary)
+    _, _, v1 = oracle.sage(pb, inp.qkv, inp.wq, inp.wk, inp.pos, kv_scale=1.0)
+    for got, full in ((qv, q1), (kv, k1), (vv, v1)):
+        assert np.array_equal(got[:, :, :17], full[:, :, :17])
+        assert np.all(got[:, :, 17:] == (0x5A5A if got.dtype == np.uint16 else np.float32(-7.25)))
+
+
+PINS += [pin_sage_vs_float64, pin_sage_v_matches_numpy, pin_sage_agrees_with_16bit_path,
+         pin_sage_kv_scale_and_prefix]

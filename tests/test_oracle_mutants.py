@@ -20,6 +20,8 @@ import pytest
 import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+# Mutant builds live inside the repository tree (git-ignored).
+_SCRATCH = os.path.join(ROOT, "tests", "_mutants")
 
 # (name, [(old, new), ...]); every `old` must occur exactly once in the source.
 MUTANTS = [
@@ -32,12 +34,12 @@ MUTANTS = [
     ("eps outside the root", [("float t = ms + eps;", "float t = ms;"),
                               ("return 1.0f / rt;", "return 1.0f / (rt + eps);")]),
     ("one rounding for 1/sqrt", [("return 1.0f / rt;", "return (float)(1.0 / sqrt((double)t));")]),
-    ("weight index", [("float y = xn * w[d];", "float y = xn * w[0];")]),
-    ("weight before the norm", [("float xn = x[d] * inv;\n        float y = xn * w[d];",
-                                 "float xn = x[d] * w[d];\n        float y = xn * inv;")]),
+    ("weight index", [("y[d] = xn * w[d];", "y[d] = xn * w[0];")]),
+    ("weight before the norm", [("float xn = x[d] * inv;\n        y[d] = xn * w[d];",
+                                 "float xn = x[d] * w[d];\n        y[d] = xn * inv;")]),
     ("K normalised with the Q weight", [("const float* w = part == 0 ? wq : wk;",
                                          "const float* w = part == 0 ? wq : wq;")]),
-    ("rotation sign", [("*u_out = h3o_round16(dtype, uc - vs);", "*u_out = h3o_round16(dtype, uc + vs);")]),
+    ("rotation sign", [("*u_out = uc - vs;", "*u_out = uc + vs;")]),
     ("rotation operand", [("float us = u * s;", "float us = v * s;")]),
     ("half-split pairs", [("h3o_rotate_pair(pb->in_dtype, cs[i], sn[i], n[2 * i], n[2 * i + 1],\n"
                            "                        &dst[2 * i], &dst[2 * i + 1]);",
@@ -86,6 +88,23 @@ MUTANTS = [
     ("residual fused", [("            float t = b * sc;\n            out[i] = residual[i] + t;",
                          "            out[i] = fmaf(b, sc, residual[i]);")]),
     ("residual scale channel", [("float sc = scale[scale_len == 1 ? 0 : c];", "float sc = scale[0];")]),
+    ("sage norm rounded to 16 bits", [("h3o_norm_head_f32(x, w, D, pb->eps, n);",
+                                       "h3o_norm_head_f32(x, w, D, pb->eps, n);\n    for (int d = 0; d < D; ++d)"
+                                       " n[d] = h3o_widen(pb->in_dtype, h3o_round16(pb->in_dtype, n[d]));")]),
+    ("sage K without kv_scale", [("out_k[o + d] = y[d] * kv_scale;", "out_k[o + d] = y[d];")]),
+    ("sage kv_scale on Q too", [("h3o_head_f32(pb, row + (int64_t)h * D, wq, cs, sn, out_q + o);",
+                                 "h3o_head_f32(pb, row + (int64_t)h * D, wq, cs, sn, out_q + o);\n"
+                                 "            for (int d = 0; d < D; ++d) out_q[o + d] *= kv_scale;")]),
+    ("sage K with the Q weight", [("h3o_head_f32(pb, row + HD + (int64_t)h * D, wk, cs, sn, y);",
+                                   "h3o_head_f32(pb, row + HD + (int64_t)h * D, wq, cs, sn, y);")]),
+    ("sage V unscaled", [("float sv = h3o_widen(pb->in_dtype, v[d]) * kv_scale;",
+                          "float sv = h3o_widen(pb->in_dtype, v[d]);")]),
+    ("sage V through bfloat16", [("out_v[o + d] = h3o_f32_to_f16(sv);",
+                                  "out_v[o + d] = h3o_f32_to_f16(h3o_bf16_to_f32(h3o_f32_to_bf16(sv)));")]),
+    ("sage half-split pairs", [("h3o_rotate_f32(cs[i], sn[i], n[2 * i], n[2 * i + 1], &dst[2 * i], &dst[2 * i + 1]);",
+                                "h3o_rotate_f32(cs[i], sn[i], n[i], n[i + R / 2], &dst[i], &dst[i + R / 2]);")]),
+    ("sage pass-through zeroed", [("memcpy(dst + R, n + R, sizeof(float) * (size_t)(D - R));",
+                                   "memset(dst + R, 0, sizeof(float) * (size_t)(D - R));")]),
     ("f16 widening bias", [("else v = ldexpf((float)(man | 0x400), ex - 25);",
                             "else v = ldexpf((float)(man | 0x400), ex - 24);")]),
 ]
@@ -123,7 +142,8 @@ def _run(name_edits):
     name, edits = name_edits
     with open(oracle._SRC) as f:
         src = f.read()
-    with tempfile.TemporaryDirectory() as d:
+    os.makedirs(_SCRATCH, exist_ok=True)
+    with tempfile.TemporaryDirectory(dir=_SCRATCH) as d:
         so = _make(src, edits, d)
         env = dict(os.environ, H3QK_ORACLE_LIB=so)
         r = subprocess.run([sys.executable, "-c", _CHILD.format(root=ROOT)], env=env,
