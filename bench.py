@@ -292,6 +292,48 @@ def adjacent_ops(dev, stream, iters: int = 20):
     return rows
 
 
+def variant_ops(dev, stream, qkv, wq, wk, pos, common, spec, iters: int = 20):
+    """Other output forms of the path on the same tile, timed after the main
+    region: the sage outputs (float32 Q, float32 K * kv_scale, float16 V *
+    kv_scale; 6 bytes read + 10 written per element) and the e4m3 cast with
+    a static scale table (6 read + 3 written)."""
+    import torch
+
+    from video_vae_decoder_qkv_gb300 import prepare, prepare_sage
+
+    N, H, D = spec.rows, spec.heads, spec.head_dim
+    shape = (1, H, N, D)
+    n = spec.valid_rows() * spec.hd
+    rows = {}
+    qs = torch.empty(shape, dtype=torch.float32, device=dev)
+    ks = torch.empty(shape, dtype=torch.float32, device=dev)
+    vs = torch.empty(shape, dtype=torch.float16, device=dev)
+    out8 = tuple(torch.empty(shape, dtype=torch.float8_e4m3fn, device=dev) for _ in range(3))
+    sc = torch.empty(3, dtype=torch.float32, device=dev)
+    table = torch.tensor([0.02, 0.02, 0.01], dtype=torch.float32, device=dev)
+    for name, fn, nbytes in (
+            ("sage_f32q_f32k_f16v", lambda: prepare_sage(qkv, wq, wk, pos, kv_scale=0.5, out=(qs, ks, vs),
+                                                         stream=stream, **common), 16 * n),
+            ("e4m3_static", lambda: prepare(qkv, wq, wk, pos, scale_mode="static", static_scales=table,
+                                            out=out8, out_scales=sc, stream=stream, **common), 9 * n)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(iters):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b))
+        ms = statistics.fmean(ts)
+        rows[name] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9, "bytes": nbytes}
+    del qs, ks, vs, out8
+    torch.cuda.empty_cache()
+    return rows
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -403,6 +445,7 @@ def run_ours(args):
     e2e_s = es.elapsed_time(ee) / 1e3
     e2e_max, e2e_bytes = reduce_max_sum(dist, e2e_s, step_bytes * E, dev)
 
+    variants = variant_ops(dev, stream, qkv, wq, wk, pos, common, spec16)
     extra = adjacent_ops(dev, stream) if not args.tokens else None
 
     cpu = None
@@ -444,6 +487,7 @@ def run_ours(args):
             "e2e": {"value": e2e_bytes / e2e_max / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": E},
             "gpu_launches": launches,
+            "variants": variants,
             "adjacent_ops": extra,
             "clocks": clocks,
             "cpu_baseline": cpu,

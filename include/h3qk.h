@@ -240,6 +240,37 @@ h3qk_status h3qk_cast(const void* qkv, const float* norm_wq, const float* norm_w
                       h3qk_stream_t stream);
 
 /*
+ * h3qk_prepare_sage: the path with the outputs a sage attention kernel reads
+ * (stable-diffusion.cpp PR #19, first commit: the fused RoPE / permute op
+ * writes head-major [head_dim, tokens, heads, batch] tensors, F32 Q, F32 K
+ * times kv_scale and F16 V times kv_scale, with the rounding points of the
+ * unfused sage chain).
+ *
+ * Arithmetic: the widened 16-bit input stays binary32 to the end: the
+ * normalised value (x * inv) * w is NOT rounded to 16 bits before the
+ * rotation; the rotated values are written as binary32 for Q, and as
+ * binary32 products with kv_scale (one rounding) for K; V is widened,
+ * multiplied by kv_scale (one binary32 rounding) and rounded to binary16
+ * (nearest even, overflow to infinity).  Norm, reduction tree, sin/cos and
+ * angles are those of h3qk_prepare.
+ *
+ * Arguments as for h3qk_prepare, except:
+ *   kv_scale   a finite binary32 factor of K and V (1 leaves them unscaled).
+ *   out_q, out_k  float [B, H, S, D] (or [B, S, H, D], opts->out_layout).
+ *   out_v      IEEE binary16 codes, same shape.
+ *   All three 16-byte aligned, pairwise disjoint and disjoint from every
+ *   input; rows past the valid prefix keep their previous bytes.
+ *   opts->in_dtype DEFAULT means BF16; opts->static_scales, workspace and
+ *   sat_counts are ignored (there is no e4m3 cast).
+ * Errors and asynchrony as for h3qk_prepare (a non-finite kv_scale is
+ * H3QK_ERR_INVALID_ARG).
+ */
+h3qk_status h3qk_prepare_sage(const void* qkv, const float* norm_wq, const float* norm_wk,
+                              const int32_t* positions, int64_t tokens, int32_t heads, int32_t head_dim,
+                              int32_t rotary_dim, int64_t valid_len, float kv_scale, float* out_q,
+                              float* out_k, void* out_v, const h3qk_opts* opts, h3qk_stream_t stream);
+
+/*
  * h3qk_prepare_noalloc: h3qk_prepare for callers that cannot allocate device
  * memory at the point of the call -- for example a plugin inside an inference
  * engine that receives all of its memory up front, or a real-time decode loop

@@ -125,6 +125,9 @@ def oracle_full(inp: W.Inputs, static=None, fill: int | None = None):
 
 
 def _nan_mask(codes: np.ndarray, kind: str) -> np.ndarray:
+    if kind == "f32":
+        c = codes.astype(np.uint32)
+        return ((c & 0x7F800000) == 0x7F800000) & ((c & 0x7FFFFF) != 0)
     if kind == "e4m3":
         return (codes & 0x7F) == 0x7F
     if kind == "fp16":

@@ -163,6 +163,35 @@ def test_split_entry_points_check_arguments(fn, kw, want):
     assert _split_call(fn, **kw) == want
 
 
+def _sage(**kw):
+    a = dict(qkv=QKV, norm_wq=WQ, norm_wk=WK, positions=POS, tokens=N, heads=H, head_dim=D,
+             rotary_dim=R, valid_len=N, kv_scale=1.0, out_q=OQ, out_k=OK_, out_v=OV)
+    a.update(kw)
+    return h3qk.prepare_sage_ptr(a["qkv"], a["norm_wq"], a["norm_wk"], a["positions"], a["tokens"], a["heads"],
+                                 a["head_dim"], a["rotary_dim"], a["valid_len"], a["kv_scale"], a["out_q"],
+                                 a["out_k"], a["out_v"], None, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(kv_scale=float("nan")), h3qk.ERR_INVALID_ARG),
+    (dict(kv_scale=float("inf")), h3qk.ERR_INVALID_ARG),
+    (dict(out_v=None), h3qk.ERR_INVALID_ARG),
+    (dict(head_dim=12), h3qk.ERR_INVALID_ARG),
+    (dict(valid_len=N + 1), h3qk.ERR_INVALID_ARG),
+    (dict(out_q=OQ + 8), h3qk.ERR_MISALIGNED),
+    (dict(out_v=OV + 2), h3qk.ERR_MISALIGNED),
+    (dict(out_k=OQ + N * H * D * 4 - 16), h3qk.ERR_ALIAS),   # K starts inside Q (4-byte elements)
+    (dict(out_v=QKV + 16), h3qk.ERR_ALIAS),
+    (dict(out_q=WQ), h3qk.ERR_ALIAS),
+])
+def test_sage_entry_point_checks_arguments(kw, want):
+    assert _sage(**kw) == want
+
+
+def test_sage_valid_call_without_a_device_reports_cuda_error():
+    assert _sage() == h3qk.ERR_CUDA
+
+
 def _vae(fn, **kw):
     L = h3qk.lib()
     if fn == "silu":

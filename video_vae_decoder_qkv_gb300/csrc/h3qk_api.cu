@@ -64,6 +64,9 @@ cudaError_t launch_mode(int mode, const h3qk::Params& p, int blocks, cudaStream_
     case h3qk::kAmax:
         h3qk::qkprep_kernel<BF16, LPR, CH, U, h3qk::kAmax><<<blocks, h3qk::kThreads, 0, st>>>(p);
         break;
+    case h3qk::kSage:
+        h3qk::qkprep_kernel<BF16, LPR, CH, U, h3qk::kSage><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        break;
     default:
         h3qk::qkprep_kernel<BF16, LPR, CH, U, h3qk::kCast><<<blocks, h3qk::kThreads, 0, st>>>(p);
         break;
@@ -525,6 +528,38 @@ h3qk_status h3qk_cast(const void* qkv, const float* norm_wq, const float* norm_w
         p.sat_counts = o.sat_counts;
     }
     const cudaError_t e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.blocks, pl.st);
+    return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
+}
+
+h3qk_status h3qk_prepare_sage(const void* qkv, const float* norm_wq, const float* norm_wk,
+                              const int32_t* positions, int64_t tokens, int32_t heads, int32_t head_dim,
+                              int32_t rotary_dim, int64_t valid_len, float kv_scale, float* out_q,
+                              float* out_k, void* out_v, const h3qk_opts* opts, h3qk_stream_t stream)
+{
+    h3qk_opts o;
+    h3qk_opts_init(&o);
+    if (opts) o = *opts;
+    Plan pl;
+    h3qk_status s = plan_inputs(qkv, norm_wq, norm_wk, positions, tokens, heads, head_dim, rotary_dim,
+                                valid_len, H3QK_BF16, o, stream, &pl);
+    if (s != H3QK_OK) return s;
+    if (!std::isfinite(kv_scale)) return H3QK_ERR_INVALID_ARG;
+    if (tokens > 0 && (!out_q || !out_k || !out_v)) return H3QK_ERR_INVALID_ARG;
+    if (!aligned(out_q, 16) || !aligned(out_k, 16) || !aligned(out_v, 16)) return H3QK_ERR_MISALIGNED;
+    const Range outs[3] = {range_of(out_q, tokens * pl.HD * 4), range_of(out_k, tokens * pl.HD * 4),
+                           range_of(out_v, tokens * pl.HD * 2)};
+    for (int i = 0; i < 3; ++i) {
+        for (int k = i + 1; k < 3; ++k)
+            if (overlap(outs[i], outs[k])) return H3QK_ERR_ALIAS;
+        if (overlaps_inputs(pl, outs[i])) return H3QK_ERR_ALIAS;
+    }
+    h3qk::Params& p = pl.p;
+    p.out[0] = out_q;
+    p.out[1] = out_k;
+    p.out[2] = out_v;
+    p.kv_scale = kv_scale;
+    if (tokens == 0 || (valid_len == 0 && !o.valid_lens)) return H3QK_OK;
+    const cudaError_t e = launch(pl.bf16, pl.P, h3qk::kSage, p, pl.blocks, pl.st);
     return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
 }
 

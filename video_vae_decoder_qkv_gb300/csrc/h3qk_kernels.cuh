@@ -52,7 +52,7 @@ constexpr int kThreads = 32 * kWarpsPerBlock;
 constexpr int kChunksPerLane = H3QK_CH;
 constexpr int kUnroll = H3QK_UNROLL;
 
-enum Mode : int { kOut16 = 0, kAmax = 1, kCast = 2 };
+enum Mode : int { kOut16 = 0, kAmax = 1, kCast = 2, kSage = 3 };
 
 // Everything a launch needs, passed as one __grid_constant__ parameter.
 struct Params {
@@ -85,6 +85,7 @@ struct Params {
     int32_t slot[3];             // amax / scale / count slot of each part, -1 if unused
     const int32_t* valid_lens;   // per-item valid lengths (device), or null
     unsigned int* sat_counts;    // cast mode: clipped-element counters (device), or null
+    float kv_scale;              // sage mode: factor of K (binary32 out) and V (binary16 out)
     float inv_freq[kMaxPairs];   // per rotary pair
     uint8_t axis[kMaxPairs];     // position axis of each rotary pair
 };
@@ -232,11 +233,8 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int i)
 // rotation, and returns the 16-bit words.
 // ---------------------------------------------------------------------------
 template <bool BF16, int LPR, int CH>
-__device__ __forceinline__ void qk_row(const uint4 (&raw)[CH], const float4* w, const float (&cs)[CH][4],
-                                       const float (&sn)[CH][4], const bool (&rot)[CH][4], float inv_d,
-                                       float eps, int D, uint32_t (&y)[CH][4])
+__device__ __forceinline__ float qk_inv(const uint4 (&raw)[CH], float inv_d, float eps, int D, float (&x)[CH][8])
 {
-    float x[CH][8];
 #pragma unroll
     for (int q = 0; q < CH; ++q)
 #pragma unroll
@@ -263,7 +261,16 @@ __device__ __forceinline__ void qk_row(const uint4 (&raw)[CH], const float4* w, 
 #pragma unroll
     for (int o = LPR / 2; o >= 1; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
     const float ms = inv_d != 0.0f ? __fmul_rn(ss, inv_d) : __fdiv_rn(ss, static_cast<float>(D));
-    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+    return __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+template <bool BF16, int LPR, int CH>
+__device__ __forceinline__ void qk_row(const uint4 (&raw)[CH], const float4* w, const float (&cs)[CH][4],
+                                       const float (&sn)[CH][4], const bool (&rot)[CH][4], float inv_d,
+                                       float eps, int D, uint32_t (&y)[CH][4])
+{
+    float x[CH][8];
+    const float inv = qk_inv<BF16, LPR, CH>(raw, inv_d, eps, D, x);
     const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
     for (int q = 0; q < CH; ++q) {
@@ -280,6 +287,61 @@ __device__ __forceinline__ void qk_row(const uint4 (&raw)[CH], const float4* w, 
             y[q][i] = rot[q][i] ? round2<BF16>(ro, rv) : n;
         }
     }
+}
+
+// The same head row for the sage outputs: every step stays binary32 (the
+// normalised value is not rounded to 16 bits before the rotation), and the
+// lane's CH*8 results are returned unrounded, chunk by chunk.
+template <bool BF16, int LPR, int CH>
+__device__ __forceinline__ void qk_row_f32(const uint4 (&raw)[CH], const float4* w, const float (&cs)[CH][4],
+                                           const float (&sn)[CH][4], const bool (&rot)[CH][4], float inv_d,
+                                           float eps, int D, float (&y)[CH][8])
+{
+    float x[CH][8];
+    const float inv = qk_inv<BF16, LPR, CH>(raw, inv_d, eps, D, x);
+    const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+    for (int q = 0; q < CH; ++q) {
+        const float4 wa = w[2 * q], wb = w[2 * q + 1];
+        const float wq[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 a = mul2(mul2(make_float2(x[q][2 * i], x[q][2 * i + 1]), inv2),
+                                  make_float2(wq[2 * i], wq[2 * i + 1]));
+            const float ro = __fsub_rn(__fmul_rn(a.x, cs[q][i]), __fmul_rn(a.y, sn[q][i]));  // u c - v s
+            const float rv = __fadd_rn(__fmul_rn(a.x, sn[q][i]), __fmul_rn(a.y, cs[q][i]));  // u s + v c
+            y[q][2 * i] = rot[q][i] ? ro : a.x;
+            y[q][2 * i + 1] = rot[q][i] ? rv : a.y;
+        }
+    }
+}
+
+// Eight binary32 values (optionally times k) -> two 16-byte stores at dst.
+__device__ __forceinline__ void store_f32x8(const float (&y)[8], float k, bool scale, float* dst)
+{
+    float2 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[i] = make_float2(y[2 * i], y[2 * i + 1]);
+        if (scale) v[i] = mul2(v[i], make_float2(k, k));
+    }
+    reinterpret_cast<float4*>(dst)[0] = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+}
+
+// Eight 16-bit values times k, each product rounded to binary32 and then to
+// binary16 (nearest even, overflow to infinity): one 16-byte store at dst.
+template <bool BF16>
+__device__ __forceinline__ void store_v_f16(const uint4& raw, float k, uint16_t* dst)
+{
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 z = mul2(widen2<BF16>(word(raw, i)), make_float2(k, k));
+        __half2 h = __floats2half2_rn(z.x, z.y);
+        o[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // Upper bound on |y| over one Q/K head row slice (amax pass early-out).
@@ -347,7 +409,8 @@ __device__ __forceinline__ void emit_e4m3(const uint32_t (&y)[4], float f, uint8
 // [B, H, S, D] or token-major [B, S, H, D]).  The reduction tree is the same for every (LPR, CH): the first
 // halving level (chunk c + chunk c+LPR) is in-lane, the rest are xor shuffles.
 // MODE kOut16 writes 16-bit head-major outputs; kAmax reduces max |y| per
-// tensor; kCast writes e4m3 codes under the dynamic or static factors.
+// tensor; kCast writes e4m3 codes under the dynamic or static factors; kSage
+// writes binary32 Q, binary32 K * kv_scale and binary16 V * kv_scale.
 // ---------------------------------------------------------------------------
 template <bool BF16, int LPR, int CH, int U, int MODE>
 __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const __grid_constant__ Params p)
@@ -486,6 +549,18 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
                         const uint32_t bb = act_row ? __float_as_uint(bnd) : 0u;
                         if (__reduce_max_sync(0xffffffffu, bb) <= run[part]) continue;  // warp-uniform
                     }
+                    if constexpr (MODE == kSage) {
+                        float yf[CH][8];
+                        qk_row_f32<BF16, LPR, CH>(rw, reinterpret_cast<const float4*>(&ws[part][c][0]), cs, sn,
+                                                  rot, p.inv_d, p.eps, D, yf);
+#pragma unroll
+                        for (int q = 0; q < CH; ++q) {
+                            if (!act[q]) continue;
+                            const int64_t off = obase + h * p.out_hstride + 8 * q * LPR;
+                            store_f32x8(yf[q], p.kv_scale, part == 1, static_cast<float*>(p.out[part]) + off);
+                        }
+                        continue;
+                    }
                     uint32_t y[CH][4];
                     qk_row<BF16, LPR, CH>(rw, reinterpret_cast<const float4*>(&ws[part][c][0]), cs, sn, rot,
                                           p.inv_d, p.eps, D, y);
@@ -534,6 +609,8 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
                         if constexpr (MODE == kOut16) {
                             uint16_t* dst = static_cast<uint16_t*>(p.out[2]) + off;
                             *reinterpret_cast<uint4*>(dst) = raw[u][q];
+                        } else if constexpr (MODE == kSage) {
+                            store_v_f16<BF16>(raw[u][q], p.kv_scale, static_cast<uint16_t*>(p.out[2]) + off);
                         } else if constexpr (MODE == kAmax) {
 #pragma unroll
                             for (int i = 0; i < 4; ++i) am[2] = hmax2_abs<BF16>(am[2], word(raw[u][q], i));

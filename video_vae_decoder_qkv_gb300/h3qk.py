@@ -217,6 +217,69 @@ def prepare(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rota
     return q, k, v, (out_scales if out_dt == E4M3 else None)
 
 
+def _sage_sig(L):
+    fn = L.h3qk_prepare_sage
+    if fn.argtypes is None:
+        P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        fn.restype = ctypes.c_int
+        fn.argtypes = [P, P, P, P, I64, I32, I32, I32, I64, ctypes.c_float, P, P, P,
+                       ctypes.POINTER(Opts), P]
+    return fn
+
+
+def prepare_sage_ptr(qkv, norm_wq, norm_wk, positions, tokens, heads, head_dim, rotary_dim, valid_len,
+                     kv_scale, out_q, out_k, out_v, opts, stream) -> int:
+    """h3qk_prepare_sage on raw device pointers (ints); returns the status."""
+    return _sage_sig(lib())(qkv, norm_wq, norm_wk, positions, tokens, heads, head_dim, rotary_dim,
+                            valid_len, kv_scale, out_q, out_k, out_v,
+                            ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def prepare_sage(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rotary_dim: int,
+                 kv_scale: float = 1.0, batch: int = 1, valid_len: int | None = None,
+                 n_axes: int | None = None, axis_dims=None, theta: float = 10000.0, eps: float = 1e-6,
+                 out=None, stream=None, out_layout: str = "head_major", valid_lens=None):
+    """The path with the outputs a sage attention kernel reads: float32 Q,
+    float32 K * kv_scale and float16 V * kv_scale, head-major [batch, heads,
+    S, head_dim] (or token-major).  Inputs as for ``prepare``.  Returns
+    (q, k, v)."""
+    import torch
+
+    if qkv.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("qkv must be float16 or bfloat16")
+    if qkv.dim() != 2 or qkv.stride(1) != 1:
+        raise ValueError("qkv must be 2-D [tokens, row_stride] with unit inner stride")
+    tokens = qkv.shape[0]
+    if tokens % batch:
+        raise ValueError("tokens must be a multiple of batch")
+    seq = tokens // batch
+    if valid_len is None:
+        valid_len = seq
+    if n_axes is None:
+        n_axes = positions.shape[1] if positions is not None and positions.dim() == 2 else 3
+    layout = {"head_major": HEAD_MAJOR, "token_major": TOKEN_MAJOR}[out_layout]
+    shape = (batch, heads, seq, head_dim) if layout == HEAD_MAJOR else (batch, seq, heads, head_dim)
+    if out is None:
+        dev = qkv.device
+        out = (torch.empty(shape, dtype=torch.float32, device=dev),
+               torch.empty(shape, dtype=torch.float32, device=dev),
+               torch.empty(shape, dtype=torch.float16, device=dev))
+    q, k, v = out
+    o = _opts_for(qkv, n_axes=n_axes, axis_dims=axis_dims, theta=theta, eps=eps, batch=batch)
+    o.out_layout = layout
+    o.valid_lens = _ptr(valid_lens)
+    if stream is None:
+        stream = torch.cuda.current_stream(qkv.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    st = prepare_sage_ptr(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens,
+                          heads, head_dim, rotary_dim, valid_len, float(kv_scale), q.data_ptr(), k.data_ptr(),
+                          v.data_ptr(), o, stream)
+    if st != OK:
+        raise H3QKError(st, status_string(st), int(lib().h3qk_last_cuda_error()))
+    return q, k, v
+
+
 def _opts_for(qkv, *, n_axes, axis_dims, theta, eps, batch):
     import torch
 
