@@ -56,19 +56,18 @@ int next_pow2(int v)
 template <bool BF16, int LPR, int CH>
 cudaError_t launch_mode(int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
 {
-    constexpr int U = h3qk::kUnroll;
     switch (mode) {
     case h3qk::kOut16:
-        h3qk::qkprep_kernel<BF16, LPR, CH, U, h3qk::kOut16><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        h3qk::qkprep_kernel<BF16, LPR, CH, h3qk::kOut16><<<blocks, h3qk::kThreads, 0, st>>>(p);
         break;
     case h3qk::kAmax:
-        h3qk::qkprep_kernel<BF16, LPR, CH, U, h3qk::kAmax><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        h3qk::qkprep_kernel<BF16, LPR, CH, h3qk::kAmax><<<blocks, h3qk::kThreads, 0, st>>>(p);
         break;
     case h3qk::kSage:
-        h3qk::qkprep_kernel<BF16, LPR, CH, U, h3qk::kSage><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        h3qk::qkprep_kernel<BF16, LPR, CH, h3qk::kSage><<<blocks, h3qk::kThreads, 0, st>>>(p);
         break;
     default:
-        h3qk::qkprep_kernel<BF16, LPR, CH, U, h3qk::kCast><<<blocks, h3qk::kThreads, 0, st>>>(p);
+        h3qk::qkprep_kernel<BF16, LPR, CH, h3qk::kCast><<<blocks, h3qk::kThreads, 0, st>>>(p);
         break;
     }
     ++g_launches;
@@ -251,6 +250,7 @@ h3qk_status plan_inputs(const void* qkv, const float* norm_wq, const float* norm
     p.in_part_off[0] = 0;
     p.in_part_off[1] = HD;
     p.in_part_off[2] = 2 * HD;
+    p.pf_span = parts * HD;
     p.qk_first = 0;
     p.qk_end = 2;
     p.has_v = 1;

@@ -34,25 +34,42 @@ constexpr int kMaxPairs = 128;       // rotary_dim <= 256
 constexpr int kWarpsPerBlock = 8;
 constexpr int kThreads = 32 * kWarpsPerBlock;
 // Tuning knobs (compile-time; the defaults are the measured best):
-// H3QK_CH chunks of 8 channels per lane (1, 2 or 4), H3QK_UNROLL Q/K head rows
-// per batch of loads, H3QK_V_UNROLL V head rows per batch, H3QK_MIN_BLOCKS resident blocks
-// per SM asked of the register allocator.
+// H3QK_CH chunks of 8 channels per lane (1, 2 or 4) for every mode, and per
+// mode a four-digit code "U UV MIN_BLOCKS PF": Q/K head rows per batch of
+// loads, V head rows per batch, resident blocks per SM asked of the register
+// allocator, and the L2 bulk prefetch distance in batches (0 = off).
 #ifndef H3QK_CH
 #define H3QK_CH 2
 #endif
-#ifndef H3QK_UNROLL
-#define H3QK_UNROLL 4
+#ifndef H3QK_TUNE_OUT16
+#define H3QK_TUNE_OUT16 4421
 #endif
-#ifndef H3QK_V_UNROLL
-#define H3QK_V_UNROLL 4
+#ifndef H3QK_TUNE_AMAX
+#define H3QK_TUNE_AMAX 2430
 #endif
-#ifndef H3QK_MIN_BLOCKS
-#define H3QK_MIN_BLOCKS 1
+#ifndef H3QK_TUNE_CAST
+#define H3QK_TUNE_CAST 2430
+#endif
+#ifndef H3QK_TUNE_SAGE
+#define H3QK_TUNE_SAGE 4410
 #endif
 constexpr int kChunksPerLane = H3QK_CH;
-constexpr int kUnroll = H3QK_UNROLL;
 
 enum Mode : int { kOut16 = 0, kAmax = 1, kCast = 2, kSage = 3 };
+
+template <int CODE>
+struct TuneT {
+    static constexpr int U = CODE / 1000;        // Q/K head rows per batch of loads
+    static constexpr int UV = CODE / 100 % 10;   // V head rows per batch
+    static constexpr int MB = CODE / 10 % 10;    // __launch_bounds__ minimum blocks per SM
+    static constexpr int PF = CODE % 10;         // L2 prefetch distance in batches
+    static_assert(U >= 1 && UV >= 1 && MB >= 1, "tuning code digits U, UV, MIN_BLOCKS must be >= 1");
+};
+template <int MODE> struct Tune;
+template <> struct Tune<kOut16> : TuneT<H3QK_TUNE_OUT16> {};
+template <> struct Tune<kAmax> : TuneT<H3QK_TUNE_AMAX> {};
+template <> struct Tune<kCast> : TuneT<H3QK_TUNE_CAST> {};
+template <> struct Tune<kSage> : TuneT<H3QK_TUNE_SAGE> {};
 
 // Everything a launch needs, passed as one __grid_constant__ parameter.
 struct Params {
@@ -86,6 +103,7 @@ struct Params {
     const int32_t* valid_lens;   // per-item valid lengths (device), or null
     unsigned int* sat_counts;    // cast mode: clipped-element counters (device), or null
     float kv_scale;              // sage mode: factor of K (binary32 out) and V (binary16 out)
+    int64_t pf_span;             // elements of an input row the call reads ([0, pf_span))
     float inv_freq[kMaxPairs];   // per rotary pair
     uint8_t axis[kMaxPairs];     // position axis of each rotary pair
 };
@@ -172,6 +190,13 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
 __device__ __forceinline__ uint4 load16(const uint16_t* p)
 {
     return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// Prefetch `bytes` bytes at p (16-byte aligned, a multiple of 16, inside the
+// input) into L2 with one bulk request; no completion is awaited.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -412,12 +437,14 @@ __device__ __forceinline__ void emit_e4m3(const uint32_t (&y)[4], float f, uint8
 // tensor; kCast writes e4m3 codes under the dynamic or static factors; kSage
 // writes binary32 Q, binary32 K * kv_scale and binary16 V * kv_scale.
 // ---------------------------------------------------------------------------
-template <bool BF16, int LPR, int CH, int U, int MODE>
-__global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const __grid_constant__ Params p)
+template <bool BF16, int LPR, int CH, int MODE>
+__global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const __grid_constant__ Params p)
 {
     static_assert(CH == 1 || CH == 2 || CH == 4, "1, 2 or 4 chunks per lane");
     constexpr int TPW = 32 / LPR;
-    constexpr int UV = H3QK_V_UNROLL;  // V head rows per batch (copy only)
+    constexpr int U = Tune<MODE>::U;    // Q/K head rows per batch of loads
+    constexpr int UV = Tune<MODE>::UV;  // V head rows per batch (copy only)
+    constexpr int PF = Tune<MODE>::PF;  // L2 prefetch distance in batches
     const int lane = threadIdx.x & 31;
     const int sub = lane / LPR;
     const int c = lane % LPR;
@@ -500,25 +527,53 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
         for (int q = 0; q < CH; ++q) act[q] = act_row && on[q];
 
         // Rotary cos / sin of this lane's pairs: pair i of chunk q is global
-        // pair 4*(c + q*LPR) + i.
+        // pair 4*(c + q*LPR) + i.  The amax pass evaluates them only when a
+        // row of the group escapes the early-out (a warp-uniform decision).
         float cs[CH][4], sn[CH][4];
         bool rot[CH][4];
 #pragma unroll
         for (int q = 0; q < CH; ++q)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int pair = 4 * (c + q * LPR) + i;
-                rot[q][i] = 2 * pair < p.rotary_dim;
+                rot[q][i] = 2 * (4 * (c + q * LPR) + i) < p.rotary_dim;
                 cs[q][i] = 1.0f;
                 sn[q][i] = 0.0f;
-                if (rot[q][i] && act[q]) {
-                    const float pv = static_cast<float>(__ldg(p.pos + r * p.n_axes + p.axis[pair]));
-                    sincos_h3(__fmul_rn(pv, p.inv_freq[pair]), sn[q][i], cs[q][i]);
-                }
             }
+        auto angles = [&]() {
+#pragma unroll
+            for (int q = 0; q < CH; ++q)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int pair = 4 * (c + q * LPR) + i;
+                    if (rot[q][i] && act[q]) {
+                        const float pv = static_cast<float>(__ldg(p.pos + r * p.n_axes + p.axis[pair]));
+                        sincos_h3(__fmul_rn(pv, p.inv_freq[pair]), sn[q][i], cs[q][i]);
+                    }
+                }
+        };
+        bool have_angles = MODE != kAmax;
+        if constexpr (MODE != kAmax) angles();
 
         const uint16_t* rowp = p.qkv + r * p.row_stride + 8 * c;
         const int64_t obase = b * p.out_bstride + s * p.out_sstride + 8 * c;
+
+        // L2 prefetch of this row's input PF batches ahead of the
+        // batch starting at element `cur`; past the row's end it continues in
+        // the row this lane handles next (grid stride).  One lane per row.
+        auto prefetch = [&](int64_t cur, int64_t n) {
+            if constexpr (PF > 0) {
+                if (c != 0) return;
+                int64_t off = cur + static_cast<int64_t>(PF) * n;
+                int64_t rr = r;
+                if (off >= p.pf_span) {
+                    off -= p.pf_span;
+                    rr += n_warps * TPW;
+                }
+                if (rr >= p.rows || off >= p.pf_span) return;
+                if (off + n > p.pf_span) n = p.pf_span - off;
+                prefetch_l2(p.qkv + rr * p.row_stride + off, static_cast<uint32_t>(2 * n));
+            }
+        };
 
         // ---- Q and K: norm + RoPE ------------------------------------------
 #pragma unroll
@@ -526,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
             if (part < p.qk_first || part >= p.qk_end) continue;  // warp-uniform
             const uint16_t* src = rowp + p.in_part_off[part];
             for (int h0 = 0; h0 < H; h0 += U) {
+                prefetch(p.in_part_off[part] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(U) * D);
                 uint4 raw[U][CH];
 #pragma unroll
                 for (int u = 0; u < U; ++u)
@@ -548,6 +604,10 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
                         const float bnd = qk_bound<BF16, LPR, CH>(rw, wmax[part], p.inv_d, p.eps, D);
                         const uint32_t bb = act_row ? __float_as_uint(bnd) : 0u;
                         if (__reduce_max_sync(0xffffffffu, bb) <= run[part]) continue;  // warp-uniform
+                        if (!have_angles) {
+                            angles();
+                            have_angles = true;
+                        }
                     }
                     if constexpr (MODE == kSage) {
                         float yf[CH][8];
@@ -589,6 +649,7 @@ __global__ void __launch_bounds__(kThreads, H3QK_MIN_BLOCKS) qkprep_kernel(const
         if (p.has_v) {
             const uint16_t* src = rowp + p.in_part_off[2];
             for (int h0 = 0; h0 < H; h0 += UV) {
+                prefetch(p.in_part_off[2] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(UV) * D);
                 uint4 raw[UV][CH];
 #pragma unroll
                 for (int u = 0; u < UV; ++u)
