@@ -53,25 +53,41 @@ int next_pow2(int v)
     return p;
 }
 
+// One launch of a mode.  Modes with a shared-memory pipeline take dynamic
+// shared memory; the kernel's dynamic limit is raised to that size once per
+// device (static and dynamic together may exceed the 48 KB default).
+template <bool BF16, int LPR, int CH, int MODE>
+cudaError_t launch_one(const h3qk::Params& p, int blocks, cudaStream_t st)
+{
+    constexpr size_t smem = h3qk::stage_bytes<CH, MODE>();
+    auto* kernel = h3qk::qkprep_kernel<BF16, LPR, CH, MODE>;
+    if constexpr (smem > 0) {
+        static std::mutex mu;
+        static bool raised[kMaxDevices] = {false};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!raised[dev]) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+            raised[dev] = true;
+        }
+    }
+    kernel<<<blocks, h3qk::kThreads, smem, st>>>(p);
+    ++g_launches;
+    return cudaGetLastError();
+}
+
 template <bool BF16, int LPR, int CH>
 cudaError_t launch_mode(int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
 {
     switch (mode) {
-    case h3qk::kOut16:
-        h3qk::qkprep_kernel<BF16, LPR, CH, h3qk::kOut16><<<blocks, h3qk::kThreads, 0, st>>>(p);
-        break;
-    case h3qk::kAmax:
-        h3qk::qkprep_kernel<BF16, LPR, CH, h3qk::kAmax><<<blocks, h3qk::kThreads, 0, st>>>(p);
-        break;
-    case h3qk::kSage:
-        h3qk::qkprep_kernel<BF16, LPR, CH, h3qk::kSage><<<blocks, h3qk::kThreads, 0, st>>>(p);
-        break;
-    default:
-        h3qk::qkprep_kernel<BF16, LPR, CH, h3qk::kCast><<<blocks, h3qk::kThreads, 0, st>>>(p);
-        break;
+    case h3qk::kOut16: return launch_one<BF16, LPR, CH, h3qk::kOut16>(p, blocks, st);
+    case h3qk::kAmax: return launch_one<BF16, LPR, CH, h3qk::kAmax>(p, blocks, st);
+    case h3qk::kSage: return launch_one<BF16, LPR, CH, h3qk::kSage>(p, blocks, st);
+    default: return launch_one<BF16, LPR, CH, h3qk::kCast>(p, blocks, st);
     }
-    ++g_launches;
-    return cudaGetLastError();
 }
 
 // P = next_pow2(D/8) chunk slots per head row: CH per lane on P/CH lanes

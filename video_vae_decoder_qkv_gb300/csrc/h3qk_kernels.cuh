@@ -35,23 +35,25 @@ constexpr int kWarpsPerBlock = 8;
 constexpr int kThreads = 32 * kWarpsPerBlock;
 // Tuning knobs (compile-time; the defaults are the measured best):
 // H3QK_CH chunks of 8 channels per lane (1, 2 or 4) for every mode, and per
-// mode a four-digit code "U UV MIN_BLOCKS PF": Q/K head rows per batch of
+// mode a five-digit code "U UV MIN_BLOCKS PF S": Q/K head rows per batch of
 // loads, V head rows per batch, resident blocks per SM asked of the register
-// allocator, and the L2 bulk prefetch distance in batches (0 = off).
+// allocator, the L2 bulk prefetch distance in batches (0 = off), and the
+// depth of the per-warp shared-memory pipeline (0 = loads straight into
+// registers; S > 0: S stages of cp.async copies, V batches of U rows).
 #ifndef H3QK_CH
 #define H3QK_CH 2
 #endif
 #ifndef H3QK_TUNE_OUT16
-#define H3QK_TUNE_OUT16 4421
+#define H3QK_TUNE_OUT16 44202
 #endif
 #ifndef H3QK_TUNE_AMAX
-#define H3QK_TUNE_AMAX 2430
+#define H3QK_TUNE_AMAX 24303
 #endif
 #ifndef H3QK_TUNE_CAST
-#define H3QK_TUNE_CAST 2430
+#define H3QK_TUNE_CAST 24303
 #endif
 #ifndef H3QK_TUNE_SAGE
-#define H3QK_TUNE_SAGE 4410
+#define H3QK_TUNE_SAGE 44204
 #endif
 constexpr int kChunksPerLane = H3QK_CH;
 
@@ -59,10 +61,11 @@ enum Mode : int { kOut16 = 0, kAmax = 1, kCast = 2, kSage = 3 };
 
 template <int CODE>
 struct TuneT {
-    static constexpr int U = CODE / 1000;        // Q/K head rows per batch of loads
-    static constexpr int UV = CODE / 100 % 10;   // V head rows per batch
-    static constexpr int MB = CODE / 10 % 10;    // __launch_bounds__ minimum blocks per SM
-    static constexpr int PF = CODE % 10;         // L2 prefetch distance in batches
+    static constexpr int U = CODE / 10000;       // Q/K head rows per batch of loads
+    static constexpr int UV = CODE / 1000 % 10;  // V head rows per batch (register path)
+    static constexpr int MB = CODE / 100 % 10;   // __launch_bounds__ minimum blocks per SM
+    static constexpr int PF = CODE / 10 % 10;    // L2 prefetch distance in batches
+    static constexpr int S = CODE % 10;          // shared-memory pipeline stages (0 = none)
     static_assert(U >= 1 && UV >= 1 && MB >= 1, "tuning code digits U, UV, MIN_BLOCKS must be >= 1");
 };
 template <int MODE> struct Tune;
@@ -70,6 +73,14 @@ template <> struct Tune<kOut16> : TuneT<H3QK_TUNE_OUT16> {};
 template <> struct Tune<kAmax> : TuneT<H3QK_TUNE_AMAX> {};
 template <> struct Tune<kCast> : TuneT<H3QK_TUNE_CAST> {};
 template <> struct Tune<kSage> : TuneT<H3QK_TUNE_SAGE> {};
+
+// Dynamic shared memory of one block of a mode: S stages x U head rows x CH
+// chunks x 32 lanes x 16 bytes per warp.
+template <int CH, int MODE>
+constexpr size_t stage_bytes()
+{
+    return static_cast<size_t>(kWarpsPerBlock) * Tune<MODE>::S * Tune<MODE>::U * CH * 32 * 16;
+}
 
 // Everything a launch needs, passed as one __grid_constant__ parameter.
 struct Params {
@@ -197,6 +208,21 @@ __device__ __forceinline__ uint4 load16(const uint16_t* p)
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// One 16-byte asynchronous copy global -> shared (L2 only, no L1 allocation),
+// and the commit / wait of the calling thread's copy groups.  A thread reads
+// back only what it copied itself, so no barrier is involved.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
+{
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(a), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -443,7 +469,8 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
     static_assert(CH == 1 || CH == 2 || CH == 4, "1, 2 or 4 chunks per lane");
     constexpr int TPW = 32 / LPR;
     constexpr int U = Tune<MODE>::U;    // Q/K head rows per batch of loads
-    constexpr int UV = Tune<MODE>::UV;  // V head rows per batch (copy only)
+    constexpr int S = Tune<MODE>::S;    // shared-memory pipeline stages (0 = none)
+    constexpr int UV = S > 0 ? U : Tune<MODE>::UV;  // V head rows per batch (copy only)
     constexpr int PF = Tune<MODE>::PF;  // L2 prefetch distance in batches
     const int lane = threadIdx.x & 31;
     const int sub = lane / LPR;
@@ -502,11 +529,83 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
 #pragma unroll
             for (int k = 0; k < CH * 8; ++k) wmax[part] = fmaxf(wmax[part], fabsf(ws[part][c][k]));
     }
-    // Warp-uniform running max of the exact |y| seen per part (binary32 bits).
+    // Warp-uniform running max of the exact |y| seen per part (binary32 bits),
+    // the part of it already published to the amax words, and the published
+    // grid-wide value read at the start of each part.  Every published value
+    // is an exact |y| of some element, so it never exceeds the final amax and
+    // rows bounded below it cannot change the result.
     uint32_t run[3] = {0u, 0u, 0u};
+    uint32_t pub[2] = {0u, 0u};
+    uint32_t thr[2] = {0u, 0u};
 
     uint32_t am[3] = {0u, 0u, 0u};  // packed 16-bit running max of |y| per tensor
     unsigned int sat[3] = {0u, 0u, 0u};
+
+    // ---- shared-memory pipeline (S > 0) -------------------------------------
+    // Each lane copies its own 16-byte chunks of the batch S-1 steps ahead
+    // into its warp's ring of S stages, walking the same sequence of batches
+    // the loop below consumes (groups, then parts Q, K, V, then head
+    // batches); stage layout [S][U][CH][32 lanes] of uint4.
+    extern __shared__ __align__(16) uint4 h3qk_stage[];
+    uint4* const ring = h3qk_stage + static_cast<size_t>(threadIdx.x >> 5) * (S > 0 ? S * U * CH * 32 : 0);
+    const int first_part = p.qk_first < p.qk_end ? p.qk_first : 2;
+    int64_t fg = warp0;          // issue cursor: group, part, first head, stage
+    int fpart = first_part, fh0 = 0, fstage = 0;
+    const uint16_t* frow = p.qkv;
+    bool fact[CH];
+    auto feed_group = [&]() {    // row pointer and active chunks of group fg
+        const int64_t rr = fg * TPW + sub;
+        bool ok = false;
+        if (rr < p.rows) {
+            const int64_t bb = rr / p.seq;
+            int64_t vl = p.valid_len;
+            if (p.valid_lens) {
+                vl = __ldg(p.valid_lens + bb);
+                vl = vl < 0 ? 0 : (vl > p.seq ? p.seq : vl);
+            }
+            ok = rr - bb * p.seq < vl;
+        }
+        frow = ok ? p.qkv + rr * p.row_stride + 8 * c : p.qkv;
+#pragma unroll
+        for (int q = 0; q < CH; ++q) fact[q] = ok && on[q];
+    };
+    auto issue = [&]() {         // copies of the next batch, one commit group
+        if constexpr (S > 0) {
+            if (fg < n_groups) {
+                uint4* st = ring + fstage * (U * CH * 32);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int q = 0; q < CH; ++q)
+                        if (fh0 + u < H && fact[q])
+                            cp_async16(st + (u * CH + q) * 32 + lane,
+                                       frow + p.in_part_off[fpart] + static_cast<int64_t>(fh0 + u) * D + 8 * q * LPR);
+                fh0 += U;
+                if (fh0 >= H) {
+                    fh0 = 0;
+                    if (fpart < 2 && fpart + 1 < p.qk_end) {
+                        ++fpart;
+                    } else if (fpart < 2 && p.has_v) {
+                        fpart = 2;
+                    } else {
+                        fpart = first_part;
+                        fg += n_warps;
+                        if (fg < n_groups) feed_group();
+                    }
+                }
+            }
+            cp_async_commit();
+            fstage = fstage + 1 == S ? 0 : fstage + 1;
+        }
+    };
+    int pstage = 0;              // stage of the batch the loop consumes next
+    if constexpr (S > 0) {
+#pragma unroll
+        for (int q = 0; q < CH; ++q) fact[q] = false;
+        if (fg < n_groups) feed_group();
+#pragma unroll 1
+        for (int k = 0; k < S - 1; ++k) issue();
+    }
 
     for (int64_t g = warp0; g < n_groups; g += n_warps) {
         const int64_t r = g * TPW + sub;
@@ -579,18 +678,35 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             if (part < p.qk_first || part >= p.qk_end) continue;  // warp-uniform
+            if constexpr (MODE == kAmax) {
+                const uint32_t gw = lane == 0 ? __ldcg(p.amax_words + p.slot[part]) : 0u;
+                thr[part] = __shfl_sync(0xffffffffu, gw, 0);
+            }
             const uint16_t* src = rowp + p.in_part_off[part];
             for (int h0 = 0; h0 < H; h0 += U) {
                 prefetch(p.in_part_off[part] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(U) * D);
                 uint4 raw[U][CH];
+                if constexpr (S > 0) {
+                    // keep the ring S-1 batches ahead, then take this batch
+                    issue();
+                    cp_async_wait<(S > 0 ? S - 1 : 0)>();
+                    const uint4* st = ring + pstage * (U * CH * 32);
 #pragma unroll
-                for (int u = 0; u < U; ++u)
+                    for (int u = 0; u < U; ++u)
 #pragma unroll
-                    for (int q = 0; q < CH; ++q) {
-                        raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
-                        if (h0 + u < H && act[q])
-                            raw[u][q] = load16(src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR);
-                    }
+                        for (int q = 0; q < CH; ++q)
+                            raw[u][q] = h0 + u < H && act[q] ? st[(u * CH + q) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                    pstage = pstage + 1 == S ? 0 : pstage + 1;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+#pragma unroll
+                        for (int q = 0; q < CH; ++q) {
+                            raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
+                            if (h0 + u < H && act[q])
+                                raw[u][q] = load16(src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR);
+                        }
+                }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int h = h0 + u;
@@ -600,10 +716,12 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
                     for (int q = 0; q < CH; ++q) rw[q] = raw[u][q];
                     if constexpr (MODE == kAmax) {
                         // Exact early-out: when no lane's bound exceeds the largest
-                        // exact |y| this warp has seen, the row cannot raise the amax.
+                        // exact |y| known (this warp's, or the grid's published
+                        // one), the row cannot raise the amax.
                         const float bnd = qk_bound<BF16, LPR, CH>(rw, wmax[part], p.inv_d, p.eps, D);
                         const uint32_t bb = act_row ? __float_as_uint(bnd) : 0u;
-                        if (__reduce_max_sync(0xffffffffu, bb) <= run[part]) continue;  // warp-uniform
+                        const uint32_t known = run[part] > thr[part] ? run[part] : thr[part];
+                        if (__reduce_max_sync(0xffffffffu, bb) <= known) continue;  // warp-uniform
                         if (!have_angles) {
                             angles();
                             have_angles = true;
@@ -639,8 +757,13 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
                                             sat[part]);
                         }
                     }
-                    if constexpr (MODE == kAmax)
+                    if constexpr (MODE == kAmax) {
                         run[part] = __reduce_max_sync(0xffffffffu, __float_as_uint(hmax2_to_float<BF16>(am[part])));
+                        if (run[part] > pub[part]) {  // warp-uniform
+                            if (lane == 0) atomicMax(p.amax_words + p.slot[part], run[part]);
+                            pub[part] = run[part];
+                        }
+                    }
                 }
             }
         }
@@ -651,14 +774,26 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
             for (int h0 = 0; h0 < H; h0 += UV) {
                 prefetch(p.in_part_off[2] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(UV) * D);
                 uint4 raw[UV][CH];
+                if constexpr (S > 0) {
+                    issue();
+                    cp_async_wait<(S > 0 ? S - 1 : 0)>();
+                    const uint4* st = ring + pstage * (U * CH * 32);
 #pragma unroll
-                for (int u = 0; u < UV; ++u)
+                    for (int u = 0; u < UV; ++u)
 #pragma unroll
-                    for (int q = 0; q < CH; ++q) {
-                        raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
-                        if (h0 + u < H && act[q])
-                            raw[u][q] = load16(src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR);
-                    }
+                        for (int q = 0; q < CH; ++q)
+                            raw[u][q] = h0 + u < H && act[q] ? st[(u * CH + q) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                    pstage = pstage + 1 == S ? 0 : pstage + 1;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < UV; ++u)
+#pragma unroll
+                        for (int q = 0; q < CH; ++q) {
+                            raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
+                            if (h0 + u < H && act[q])
+                                raw[u][q] = load16(src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR);
+                        }
+                }
 #pragma unroll
                 for (int u = 0; u < UV; ++u) {
                     const int h = h0 + u;
@@ -684,6 +819,8 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
             }
         }
     }
+
+    if constexpr (S > 0) cp_async_wait<0>();  // only empty groups remain; keep the exit clean
 
     if constexpr (MODE == kAmax) {
         __shared__ float red[3][kWarpsPerBlock];
