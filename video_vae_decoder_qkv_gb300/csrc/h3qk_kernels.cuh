@@ -429,11 +429,11 @@ __device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, fl
     return 1.45f * inv * hmax2_to_float<BF16>(m2) * wmax + 0x1p-23f;
 }
 
-// Eight 16-bit values -> eight e4m3 codes at dst (8 bytes); counts the values
-// whose scaled magnitude exceeds 448 (clipped to the largest code) into *sat.
-template <bool BF16>
-__device__ __forceinline__ void emit_e4m3(const uint32_t (&y)[4], float f, uint8_t* dst, bool count,
-                                          unsigned int& sat)
+// Eight 16-bit values -> eight e4m3 codes at dst (8 bytes); with COUNT, adds
+// the number of values whose scaled magnitude exceeds 448 (clipped to the
+// largest code) to sat.
+template <bool BF16, bool COUNT>
+__device__ __forceinline__ void emit_e4m3(const uint32_t (&y)[4], float f, uint8_t* dst, unsigned int& sat)
 {
     const float2 fa = make_float2(f, f);
     uint32_t cw[2];
@@ -442,7 +442,7 @@ __device__ __forceinline__ void emit_e4m3(const uint32_t (&y)[4], float f, uint8
         const float2 z0 = mul2(widen2<BF16>(y[2 * i]), fa);
         const float2 z1 = mul2(widen2<BF16>(y[2 * i + 1]), fa);
         cw[i] = e4m3x2(z0.x, z0.y) | (e4m3x2(z1.x, z1.y) << 16);
-        if (count)
+        if constexpr (COUNT)
             sat += (fabsf(z0.x) > 448.0f) + (fabsf(z0.y) > 448.0f) + (fabsf(z1.x) > 448.0f) +
                    (fabsf(z1.y) > 448.0f);
     }
@@ -687,7 +687,11 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
                 prefetch(p.in_part_off[part] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(U) * D);
                 uint4 raw[U][CH];
                 if constexpr (S > 0) {
-                    // keep the ring S-1 batches ahead, then take this batch
+                    // Keep the ring S-1 batches ahead, then take this batch.  Only
+                    // chunks past the head are zeroed (they pad the reduction); a
+                    // padded row's or a missing head's slot holds stale bytes, which
+                    // never reach a store, the amax or a count (every use is masked
+                    // by act / the head loop, and the amax bound of such a row is 0).
                     issue();
                     cp_async_wait<(S > 0 ? S - 1 : 0)>();
                     const uint4* st = ring + pstage * (U * CH * 32);
@@ -695,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
                     for (int u = 0; u < U; ++u)
 #pragma unroll
                         for (int q = 0; q < CH; ++q)
-                            raw[u][q] = h0 + u < H && act[q] ? st[(u * CH + q) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                            raw[u][q] = on[q] ? st[(u * CH + q) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
                     pstage = pstage + 1 == S ? 0 : pstage + 1;
                 } else {
 #pragma unroll
@@ -753,8 +757,11 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
 #pragma unroll
                             for (int i = 0; i < 4; ++i) am[part] = hmax2_abs<BF16>(am[part], y[q][i]);
                         } else {
-                            emit_e4m3<BF16>(y[q], fac[part], static_cast<uint8_t*>(p.out[part]) + off, count_sat,
-                                            sat[part]);
+                            uint8_t* dst = static_cast<uint8_t*>(p.out[part]) + off;
+                            if (count_sat)  // warp-uniform
+                                emit_e4m3<BF16, true>(y[q], fac[part], dst, sat[part]);
+                            else
+                                emit_e4m3<BF16, false>(y[q], fac[part], dst, sat[part]);
                         }
                     }
                     if constexpr (MODE == kAmax) {
@@ -782,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
                     for (int u = 0; u < UV; ++u)
 #pragma unroll
                         for (int q = 0; q < CH; ++q)
-                            raw[u][q] = h0 + u < H && act[q] ? st[(u * CH + q) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                            raw[u][q] = on[q] ? st[(u * CH + q) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
                     pstage = pstage + 1 == S ? 0 : pstage + 1;
                 } else {
 #pragma unroll
@@ -812,7 +819,11 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
                             for (int i = 0; i < 4; ++i) am[2] = hmax2_abs<BF16>(am[2], word(raw[u][q], i));
                         } else {
                             const uint32_t yv[4] = {raw[u][q].x, raw[u][q].y, raw[u][q].z, raw[u][q].w};
-                            emit_e4m3<BF16>(yv, fac[2], static_cast<uint8_t*>(p.out[2]) + off, count_sat, sat[2]);
+                            uint8_t* dst = static_cast<uint8_t*>(p.out[2]) + off;
+                            if (count_sat)  // warp-uniform
+                                emit_e4m3<BF16, true>(yv, fac[2], dst, sat[2]);
+                            else
+                                emit_e4m3<BF16, false>(yv, fac[2], dst, sat[2]);
                         }
                     }
                 }
