@@ -105,3 +105,93 @@ def test_amax_early_out_is_exact(pattern, dtype):
     torch.cuda.synchronize()
     ref = oracle.amax(G.problem(spec), qkv, inp.wq, inp.wk, inp.pos, threads=G.THREADS)
     assert np.array_equal(a.cpu().numpy().view(np.uint32), ref.view(np.uint32)), (a.cpu().numpy(), ref)
+
+
+def _sumsq_tree(x):
+    """Sum of squares of one 128-channel row in the oracle's order (chunks of
+    8 left to right, then the halving tree over 16 chunk sums), binary32."""
+    f32 = np.float32
+    p = []
+    for c in range(16):
+        acc = f32(x[8 * c] * x[8 * c])
+        for k in range(1, 8):
+            acc = f32(acc + f32(x[8 * c + k] * x[8 * c + k]))
+        p.append(acc)
+    o = 8
+    while o >= 1:
+        for i in range(o):
+            p[i] = f32(p[i] + p[i + o])
+        o //= 2
+    return p[0]
+
+
+def _sumsq_fused(x):
+    """The same sum in the order of the amax pass's bound at head_dim 128 (8
+    lanes of two chunks; fused multiply-adds over even and odd channels, one
+    add, then three xor-shuffle levels), binary32."""
+    f32 = np.float32
+    lanes = []
+    for c in range(8):
+        ax, ay = f32(0), f32(0)
+        for ch in (c, c + 8):
+            for i in range(4):
+                a, b = float(x[8 * ch + 2 * i]), float(x[8 * ch + 2 * i + 1])
+                ax = f32(float(ax) + a * a)
+                ay = f32(float(ay) + b * b)
+        lanes.append(f32(ax + ay))
+    for o in (4, 2, 1):
+        lanes = [f32(lanes[c] + lanes[c ^ o]) for c in range(8)]
+    return lanes[0]
+
+
+def _overflow_row(seed=0):
+    """A bf16 head row whose squares sum to exactly FLT_MAX in the oracle's
+    order while the bound's fused order rounds the same sum to infinity:
+    3 copies of 2^(52+k), k = 0..11 (squares 2^(104+2k), summing to
+    (2^24 - 1) 2^104 = FLT_MAX with no rounding), plus a few elements whose
+    squares sit just below half an ulp of FLT_MAX."""
+    import warnings
+
+    rng = np.random.default_rng(seed)
+    big = [2.0 ** (52 + k) for k in range(12) for _ in range(3)]
+    with warnings.catch_warnings(), np.errstate(over="ignore"):
+        warnings.simplefilter("ignore")
+        for _ in range(20000):
+            x = np.zeros(128)
+            pos = rng.permutation(128)
+            x[pos[:36]] = big
+            for j in range(int(rng.integers(2, 6))):
+                x[pos[36 + j]] = (int(rng.integers(128, 256)) / 128.0) * 2.0 ** int(rng.integers(49, 51))
+            if np.isfinite(_sumsq_tree(x)) and not np.isfinite(_sumsq_fused(x)):
+                return x.astype(np.float32)
+    raise AssertionError("no near-overflow row found")
+
+
+def test_amax_bound_near_binary32_overflow():
+    """A row whose approximate sum of squares overflows while the exact one
+    does not must not be skipped: its exact values (about 5 x the weight)
+    are the Q amax here, above every ordinary row, and come after earlier
+    rows of the same warp have set a positive running max."""
+    import torch
+
+    spec = W.LATENT_65K.with_(name="ovf", batch=1, seq=64, grid=(1, 8, 8), valid_len=64, in_dtype=W.BF16,
+                              outlier_frac=0.0, out_kind=W.OUT_E4M3, scale_mode=W.SCALE_DYNAMIC)
+    inp = G.inputs(spec)
+    vals = (inp.qkv.astype(np.uint32) << 16).view(np.float32).copy()
+    base = oracle.amax(G.problem(spec), inp.qkv, inp.wq, inp.wk, inp.pos, threads=G.THREADS)
+    row = _overflow_row()
+    # The skip decision is taken per warp over the 4 token rows it holds at
+    # head_dim 128; the other 3 rows get a flat head (small bounds) so that
+    # the decision hinges on the near-overflow row's own bound.
+    for r, h in ((1, 3), (6, 17), (33, 9)):     # Q heads after head 0 of the same rows
+        g0 = r - r % 4
+        vals[g0:g0 + 4, h * 128:(h + 1) * 128] = 1.0
+        vals[r, h * 128:(h + 1) * 128] = row
+    qkv = oracle.f32_to_bf16(vals).reshape(inp.qkv.shape)
+    mod = W.Inputs(spec, qkv, inp.wq, inp.wk, inp.pos, inp.static_scales)
+    dev = G.to_device(mod)
+    a = h3_amax(*dev, **_kw(spec))
+    torch.cuda.synchronize()
+    ref = oracle.amax(G.problem(spec), qkv, inp.wq, inp.wk, inp.pos, threads=G.THREADS)
+    assert ref[0] > base[0], (ref, base)     # the near-overflow rows hold the Q amax
+    assert np.array_equal(a.cpu().numpy().view(np.uint32), ref.view(np.uint32)), (a.cpu().numpy(), ref)

@@ -43,6 +43,7 @@ constexpr int kThreads = 32 * kWarpsPerBlock;
 #ifndef H3QK_CH
 #define H3QK_CH 2
 #endif
+
 #ifndef H3QK_TUNE_OUT16
 #define H3QK_TUNE_OUT16 44202
 #endif
@@ -407,7 +408,12 @@ __device__ __forceinline__ void store_v_f16(const uint4& raw, float k, uint16_t*
 // within 2^-19 relative of the exact inv, and takes 1.45 and 2^-23, a margin
 // of 1.7 % over the exact bound.  max|x| comes from the packed 16-bit inputs
 // (exact), max|w| is the lane's largest weight.  A NaN or infinite input gives
-// a NaN or infinite bound, which never allows a skip.
+// a NaN or infinite bound, which never allows a skip.  So does an approximate
+// sum of squares at or above 2^126: near the binary32 overflow the two
+// summation orders may round to different sides of FLT_MAX, and an infinite
+// approximate sum would otherwise give inv = 0 and a bound of 2^-23 for a row
+// whose exact values are not small.  Below 2^126 the exact sum cannot
+// overflow, and the error analysis above holds.
 template <bool BF16, int LPR, int CH>
 __device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, float inv_d, float eps, int D)
 {
@@ -425,6 +431,7 @@ __device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, fl
     float ss = acc.x + acc.y;
 #pragma unroll
     for (int o = LPR / 2; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (!(ss < 0x1p126f)) return __int_as_float(0x7f800000);  // +inf: never skip
     const float inv = rsqrtf(ss * (inv_d != 0.0f ? inv_d : 1.0f / static_cast<float>(D)) + eps);
     return 1.45f * inv * hmax2_to_float<BF16>(m2) * wmax + 0x1p-23f;
 }
@@ -678,13 +685,17 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             if (part < p.qk_first || part >= p.qk_end) continue;  // warp-uniform
-            if constexpr (MODE == kAmax) {
-                const uint32_t gw = lane == 0 ? __ldcg(p.amax_words + p.slot[part]) : 0u;
-                thr[part] = __shfl_sync(0xffffffffu, gw, 0);
-            }
             const uint16_t* src = rowp + p.in_part_off[part];
             for (int h0 = 0; h0 < H; h0 += U) {
                 prefetch(p.in_part_off[part] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(U) * D);
+                if constexpr (MODE == kAmax) {
+                    // Once per part: re-reading every batch made the three amax
+                    // words a hot spot for every warp of the grid.
+                    if (h0 == 0) {
+                        const uint32_t gw = lane == 0 ? __ldcg(p.amax_words + p.slot[part]) : 0u;
+                        thr[part] = __shfl_sync(0xffffffffu, gw, 0);
+                    }
+                }
                 uint4 raw[U][CH];
                 if constexpr (S > 0) {
                     // Keep the ring S-1 batches ahead, then take this batch.  Only
