@@ -195,3 +195,44 @@ def test_amax_bound_near_binary32_overflow():
     ref = oracle.amax(G.problem(spec), qkv, inp.wq, inp.wk, inp.pos, threads=G.THREADS)
     assert ref[0] > base[0], (ref, base)     # the near-overflow rows hold the Q amax
     assert np.array_equal(a.cpu().numpy().view(np.uint32), ref.view(np.uint32)), (a.cpu().numpy(), ref)
+
+
+def test_amax_bound_with_subnormal_squares():
+    """eps = 0 and bf16 rows whose squares fall in the binary32 subnormal
+    range (random values near 2^-75 ... 2^-72: squares of a fraction to a few
+    dozen quanta, where the bound's fused order and the oracle's order round
+    differently and the exact path's own mean square is only a few quanta).
+    Such rows never take the early-out (their sum under the root is below
+    2^-96), so they sit beside flat warp-mates here and the amax, the
+    descales and the e4m3 codes of the dynamic call must equal the
+    oracle's."""
+    import torch
+
+    spec = W.LATENT_65K.with_(name="sub", batch=1, seq=64, grid=(4, 4, 4), valid_len=64, in_dtype=W.BF16,
+                              outlier_frac=0.0, eps=0.0, out_kind=W.OUT_E4M3, scale_mode=W.SCALE_DYNAMIC)
+    inp = G.inputs(spec)
+    vals = (inp.qkv.astype(np.uint32) << 16).view(np.float32).copy()
+    rng = np.random.default_rng(4)
+    placements = [((17, 3), -75), ((22, 5), -74), ((41, 2), -73), ((46, 14), -72), ((53, 9), -74)]
+    for (r, h), e in placements:
+        g0 = r - r % 4
+        vals[g0:g0 + 4, h * 128:(h + 1) * 128] = 1.0
+        mant = 1.0 + rng.integers(0, 128, 128) / 128.0
+        expo = e + rng.integers(-1, 1, 128)
+        sign = np.where(rng.random(128) < 0.5, -1.0, 1.0)
+        vals[r, h * 128:(h + 1) * 128] = (sign * mant * 2.0 ** expo).astype(np.float32)
+    qkv = oracle.f32_to_bf16(vals).reshape(inp.qkv.shape)
+    mod = W.Inputs(spec, qkv, inp.wq, inp.wk, inp.pos, inp.static_scales)
+    dev = G.to_device(mod)
+    a = h3_amax(*dev, **_kw(spec))
+    torch.cuda.synchronize()
+    pb = G.problem(spec)
+    ref = oracle.amax(pb, qkv, inp.wq, inp.wk, inp.pos, threads=G.THREADS)
+    assert np.array_equal(a.cpu().numpy().view(np.uint32), ref.view(np.uint32)), (a.cpu().numpy(), ref)
+    q, k, v, sc = G.gpu_prepare(mod, dev=dev, fill=0xA5)
+    want = oracle.prepare(pb, qkv, inp.wq, inp.wk, inp.pos,
+                          out=tuple(np.full((1, spec.heads, spec.seq, spec.head_dim), 0xA5, np.uint8)
+                                    for _ in range(3)), threads=G.THREADS)
+    for name, g_, w_ in zip("qkv", (q, k, v), want[:3]):
+        G.assert_codes_equal(G.host_codes(g_), w_, f"subnormal rows {name}", nan_kind="e4m3")
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), want[3].view(np.uint32))

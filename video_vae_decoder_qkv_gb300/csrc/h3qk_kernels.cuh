@@ -413,7 +413,12 @@ __device__ __forceinline__ void store_v_f16(const uint4& raw, float k, uint16_t*
 // summation orders may round to different sides of FLT_MAX, and an infinite
 // approximate sum would otherwise give inv = 0 and a bound of 2^-23 for a row
 // whose exact values are not small.  Below 2^126 the exact sum cannot
-// overflow, and the error analysis above holds.
+// overflow, and the error analysis above holds.  At the other end, a sum
+// under the root (ss/D + eps) below 2^-96 also gives an infinite bound: with
+// eps = 0 and squares in the binary32 subnormal range, the two orders can
+// differ by a subnormal quantum, a large relative error when the whole sum is
+// a few quanta (and a rotated pair of such a row reaches ordinary sizes).
+// Above 2^-96 those absolute differences are below 2^-40 relative.
 template <bool BF16, int LPR, int CH>
 __device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, float inv_d, float eps, int D)
 {
@@ -432,7 +437,9 @@ __device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, fl
 #pragma unroll
     for (int o = LPR / 2; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (!(ss < 0x1p126f)) return __int_as_float(0x7f800000);  // +inf: never skip
-    const float inv = rsqrtf(ss * (inv_d != 0.0f ? inv_d : 1.0f / static_cast<float>(D)) + eps);
+    const float t = ss * (inv_d != 0.0f ? inv_d : 1.0f / static_cast<float>(D)) + eps;
+    if (!(t >= 0x1p-96f)) return __int_as_float(0x7f800000);  // +inf: never skip
+    const float inv = rsqrtf(t);
     return 1.45f * inv * hmax2_to_float<BF16>(m2) * wmax + 0x1p-23f;
 }
 
