@@ -53,11 +53,14 @@ int next_pow2(int v)
     return p;
 }
 
-// One launch of a mode.  Modes with a shared-memory pipeline take dynamic
-// shared memory; the kernel's dynamic limit is raised to that size once per
-// device (static and dynamic together may exceed the 48 KB default).
+// One launch of a mode.  The grid covers the call's row groups (32/LPR
+// token rows per warp, 8 warps per block), capped at 8 blocks per SM; the
+// kernel grid-strides over the rest.  Modes with a shared-memory pipeline
+// take dynamic shared memory; the kernel's dynamic limit is raised to that
+// size once per device (static and dynamic together may exceed the 48 KB
+// default).
 template <bool BF16, int LPR, int CH, int MODE>
-cudaError_t launch_one(const h3qk::Params& p, int blocks, cudaStream_t st)
+cudaError_t launch_one(const h3qk::Params& p, cudaStream_t st)
 {
     constexpr size_t smem = h3qk::stage_bytes<CH, MODE>();
     auto* kernel = h3qk::qkprep_kernel<BF16, LPR, CH, MODE>;
@@ -74,45 +77,51 @@ cudaError_t launch_one(const h3qk::Params& p, int blocks, cudaStream_t st)
             raised[dev] = true;
         }
     }
+    constexpr int64_t tpw = 32 / LPR;
+    const int64_t groups = (p.rows + tpw - 1) / tpw;
+    const int64_t want = (groups + h3qk::kWarpsPerBlock - 1) / h3qk::kWarpsPerBlock;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+    const int blocks = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
     kernel<<<blocks, h3qk::kThreads, smem, st>>>(p);
     ++g_launches;
     return cudaGetLastError();
 }
 
-template <bool BF16, int LPR, int CH>
-cudaError_t launch_mode(int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
+// P = next_pow2(D/8) chunk slots per head row: the mode's CH per lane on
+// P/CH lanes (fewer per lane when P < CH).
+template <bool BF16, int MODE>
+cudaError_t launch_p(int P, const h3qk::Params& p, cudaStream_t st)
 {
-    switch (mode) {
-    case h3qk::kOut16: return launch_one<BF16, LPR, CH, h3qk::kOut16>(p, blocks, st);
-    case h3qk::kAmax: return launch_one<BF16, LPR, CH, h3qk::kAmax>(p, blocks, st);
-    case h3qk::kSage: return launch_one<BF16, LPR, CH, h3qk::kSage>(p, blocks, st);
-    default: return launch_one<BF16, LPR, CH, h3qk::kCast>(p, blocks, st);
-    }
-}
-
-// P = next_pow2(D/8) chunk slots per head row: CH per lane on P/CH lanes
-// (fewer per lane when P < CH).
-template <bool BF16>
-cudaError_t launch_p(int P, int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
-{
-    constexpr int CH = h3qk::kChunksPerLane;
+    constexpr int CH = h3qk::Tune<MODE>::CH;
+    static_assert(CH == 1 || CH == 2 || CH == 4, "1, 2 or 4 chunks per lane");
     if (P < CH) {
-        if (P == 1) return launch_mode<BF16, 1, 1>(mode, p, blocks, st);
-        return launch_mode<BF16, 1, 2>(mode, p, blocks, st);  // P == 2 < CH == 4
+        if (P == 1) return launch_one<BF16, 1, 1, MODE>(p, st);
+        return launch_one<BF16, 1, 2, MODE>(p, st);  // P == 2 < CH == 4
     }
     switch (P / CH) {
-    case 1: return launch_mode<BF16, 1, CH>(mode, p, blocks, st);
-    case 2: return launch_mode<BF16, 2, CH>(mode, p, blocks, st);
-    case 4: return launch_mode<BF16, 4, CH>(mode, p, blocks, st);
-    case 8: return launch_mode<BF16, 8, CH>(mode, p, blocks, st);
-    case 16: return launch_mode<BF16, 16, CH>(mode, p, blocks, st);
-    default: return launch_mode<BF16, 32 / CH, CH>(mode, p, blocks, st);
+    case 1: return launch_one<BF16, 1, CH, MODE>(p, st);
+    case 2: return launch_one<BF16, 2, CH, MODE>(p, st);
+    case 4: return launch_one<BF16, 4, CH, MODE>(p, st);
+    case 8: return launch_one<BF16, 8, CH, MODE>(p, st);
+    case 16: return launch_one<BF16, 16, CH, MODE>(p, st);
+    default: return launch_one<BF16, 32 / CH, CH, MODE>(p, st);
     }
 }
 
-cudaError_t launch(bool bf16, int P, int mode, const h3qk::Params& p, int blocks, cudaStream_t st)
+template <bool BF16>
+cudaError_t launch_m(int P, int mode, const h3qk::Params& p, cudaStream_t st)
 {
-    return bf16 ? launch_p<true>(P, mode, p, blocks, st) : launch_p<false>(P, mode, p, blocks, st);
+    switch (mode) {
+    case h3qk::kOut16: return launch_p<BF16, h3qk::kOut16>(P, p, st);
+    case h3qk::kAmax: return launch_p<BF16, h3qk::kAmax>(P, p, st);
+    case h3qk::kSage: return launch_p<BF16, h3qk::kSage>(P, p, st);
+    default: return launch_p<BF16, h3qk::kCast>(P, p, st);
+    }
+}
+
+cudaError_t launch(bool bf16, int P, int mode, const h3qk::Params& p, cudaStream_t st)
+{
+    return bf16 ? launch_m<true>(P, mode, p, st) : launch_m<false>(P, mode, p, st);
 }
 
 h3qk_status fail_cuda(cudaError_t e)
@@ -176,7 +185,6 @@ struct Plan {
     h3qk::Params p;
     bool bf16 = false;
     int P = 1;
-    int blocks = 1;
     cudaStream_t st = nullptr;
     Range ins[5];  // qkv, norm_wq, norm_wk, positions, valid_lens
     int64_t HD = 0;
@@ -293,12 +301,6 @@ h3qk_status plan_inputs(const void* qkv, const float* norm_wq, const float* norm
         }
 
     plan->P = next_pow2(head_dim / 8);
-    const int lpr = plan->P <= h3qk::kChunksPerLane ? 1 : plan->P / h3qk::kChunksPerLane;
-    const int64_t tpw = 32 / lpr;
-    const int64_t groups = (tokens + tpw - 1) / tpw;
-    const int64_t want = (groups + h3qk::kWarpsPerBlock - 1) / h3qk::kWarpsPerBlock;
-    const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
-    plan->blocks = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
     plan->st = reinterpret_cast<cudaStream_t>(stream);
     plan->bf16 = in_dtype == H3QK_BF16;
     return H3QK_OK;
@@ -320,7 +322,7 @@ h3qk_status run_amax(const Plan& pl)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e);
     if (pl.p.rows > 0 && (pl.p.valid_len > 0 || pl.p.valid_lens)) {
-        e = launch(pl.bf16, pl.P, h3qk::kAmax, pl.p, pl.blocks, pl.st);
+        e = launch(pl.bf16, pl.P, h3qk::kAmax, pl.p, pl.st);
         if (e != cudaSuccess) return fail_cuda(e);
     }
     return H3QK_OK;
@@ -396,14 +398,14 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
     cudaError_t e;
     if (!e4m3) {
         if (tokens == 0 || (valid_len == 0 && !o.valid_lens)) return H3QK_OK;
-        e = launch(pl.bf16, pl.P, h3qk::kOut16, p, pl.blocks, pl.st);
+        e = launch(pl.bf16, pl.P, h3qk::kOut16, p, pl.st);
         return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
     }
     if (scale_mode == H3QK_SCALE_DYNAMIC) {
         s = run_amax(pl);
         if (s != H3QK_OK) return s;
     }
-    e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.blocks, pl.st);
+    e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.st);
     return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
 }
 
@@ -493,14 +495,14 @@ h3qk_status h3qk_norm_rope_tensor(const void* x, const float* norm_w, const int3
     cudaError_t e;
     if (!e4m3) {
         if (tokens == 0 || (valid_len == 0 && !o.valid_lens)) return H3QK_OK;
-        e = launch(pl.bf16, pl.P, h3qk::kOut16, p, pl.blocks, pl.st);
+        e = launch(pl.bf16, pl.P, h3qk::kOut16, p, pl.st);
         return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
     }
     if (scale_mode == H3QK_SCALE_DYNAMIC) {
         s = run_amax(pl);
         if (s != H3QK_OK) return s;
     }
-    e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.blocks, pl.st);
+    e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.st);
     return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
 }
 
@@ -543,7 +545,7 @@ h3qk_status h3qk_cast(const void* qkv, const float* norm_wq, const float* norm_w
             if (overlap(outs[i], range_of(o.sat_counts, 12))) return H3QK_ERR_ALIAS;
         p.sat_counts = o.sat_counts;
     }
-    const cudaError_t e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.blocks, pl.st);
+    const cudaError_t e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.st);
     return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
 }
 
@@ -575,7 +577,7 @@ h3qk_status h3qk_prepare_sage(const void* qkv, const float* norm_wq, const float
     p.out[2] = out_v;
     p.kv_scale = kv_scale;
     if (tokens == 0 || (valid_len == 0 && !o.valid_lens)) return H3QK_OK;
-    const cudaError_t e = launch(pl.bf16, pl.P, h3qk::kSage, p, pl.blocks, pl.st);
+    const cudaError_t e = launch(pl.bf16, pl.P, h3qk::kSage, p, pl.st);
     return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
 }
 

@@ -34,14 +34,26 @@ constexpr int kMaxPairs = 128;       // rotary_dim <= 256
 constexpr int kWarpsPerBlock = 8;
 constexpr int kThreads = 32 * kWarpsPerBlock;
 // Tuning knobs (compile-time; the defaults are the measured best):
-// H3QK_CH chunks of 8 channels per lane (1, 2 or 4) for every mode, and per
-// mode a five-digit code "U UV MIN_BLOCKS PF S": Q/K head rows per batch of
+// H3QK_CH_<MODE> chunks of 8 channels per lane (1, 2 or 4; default H3QK_CH),
+// and per mode a five-digit code "U UV MIN_BLOCKS PF S": Q/K head rows per batch of
 // loads, V head rows per batch, resident blocks per SM asked of the register
 // allocator, the L2 bulk prefetch distance in batches (0 = off), and the
 // depth of the per-warp shared-memory pipeline (0 = loads straight into
 // registers; S > 0: S stages of cp.async copies, V batches of U rows).
 #ifndef H3QK_CH
 #define H3QK_CH 2
+#endif
+#ifndef H3QK_CH_OUT16
+#define H3QK_CH_OUT16 H3QK_CH
+#endif
+#ifndef H3QK_CH_AMAX
+#define H3QK_CH_AMAX H3QK_CH
+#endif
+#ifndef H3QK_CH_CAST
+#define H3QK_CH_CAST H3QK_CH
+#endif
+#ifndef H3QK_CH_SAGE
+#define H3QK_CH_SAGE H3QK_CH
 #endif
 
 #ifndef H3QK_TUNE_OUT16
@@ -56,12 +68,12 @@ constexpr int kThreads = 32 * kWarpsPerBlock;
 #ifndef H3QK_TUNE_SAGE
 #define H3QK_TUNE_SAGE 44204
 #endif
-constexpr int kChunksPerLane = H3QK_CH;
 
 enum Mode : int { kOut16 = 0, kAmax = 1, kCast = 2, kSage = 3 };
 
-template <int CODE>
+template <int CODE, int CH_>
 struct TuneT {
+    static constexpr int CH = CH_;               // chunks of 8 channels per lane
     static constexpr int U = CODE / 10000;       // Q/K head rows per batch of loads
     static constexpr int UV = CODE / 1000 % 10;  // V head rows per batch (register path)
     static constexpr int MB = CODE / 100 % 10;   // __launch_bounds__ minimum blocks per SM
@@ -70,10 +82,10 @@ struct TuneT {
     static_assert(U >= 1 && UV >= 1 && MB >= 1, "tuning code digits U, UV, MIN_BLOCKS must be >= 1");
 };
 template <int MODE> struct Tune;
-template <> struct Tune<kOut16> : TuneT<H3QK_TUNE_OUT16> {};
-template <> struct Tune<kAmax> : TuneT<H3QK_TUNE_AMAX> {};
-template <> struct Tune<kCast> : TuneT<H3QK_TUNE_CAST> {};
-template <> struct Tune<kSage> : TuneT<H3QK_TUNE_SAGE> {};
+template <> struct Tune<kOut16> : TuneT<H3QK_TUNE_OUT16, H3QK_CH_OUT16> {};
+template <> struct Tune<kAmax> : TuneT<H3QK_TUNE_AMAX, H3QK_CH_AMAX> {};
+template <> struct Tune<kCast> : TuneT<H3QK_TUNE_CAST, H3QK_CH_CAST> {};
+template <> struct Tune<kSage> : TuneT<H3QK_TUNE_SAGE, H3QK_CH_SAGE> {};
 
 // Dynamic shared memory of one block of a mode: S stages x U head rows x CH
 // chunks x 32 lanes x 16 bytes per warp.
