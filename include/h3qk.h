@@ -271,6 +271,51 @@ h3qk_status h3qk_prepare_sage(const void* qkv, const float* norm_wq, const float
                               float* out_k, void* out_v, const h3qk_opts* opts, h3qk_stream_t stream);
 
 /*
+ * h3qk_prepare_host: h3qk_prepare on HOST buffers.  The inputs (qkv,
+ * norm_wq, norm_wk, positions, opts->static_scales, opts->valid_lens) and
+ * the outputs (out_q, out_k, out_v, out_scales) are host memory, laid out as
+ * for h3qk_prepare; page-locked (pinned) memory lets the copies run
+ * asynchronously and overlap, pageable memory works but serialises them.
+ * The pages move the fused op's inputs and outputs as device tensors; this
+ * entry adds the transfers for callers whose tensors live on the host, the
+ * whole round trip being one library call.
+ *
+ * The call is cut into chunks of at most 8,192 token rows inside one item.
+ * Three streams owned by the library (created on the first call on each
+ * device) copy a chunk in, compute it and copy it out, so the transfers of
+ * one chunk overlap the kernels and transfers of others.  In dynamic e4m3
+ * mode every chunk goes through the amax pass as it arrives and the cast
+ * pass follows once all have arrived.  Only valid rows are copied: output
+ * rows past the valid prefix keep their previous bytes on the host.
+ *
+ *   workspace        device memory, 256-byte aligned, of at least
+ *                    h3qk_host_workspace_bytes() bytes for this call shape:
+ *                    the weights, a ring of three chunk slots (dynamic
+ *                    e4m3: the whole input, which the cast pass reads after
+ *                    the amax pass) and the descales.  Calls that share a
+ *                    workspace must be ordered (one caller stream).
+ *   opts             as for h3qk_prepare, except that static_scales and
+ *                    valid_lens are host arrays, and sat_counts and
+ *                    opts->workspace must be NULL.
+ *   stream           the call starts after the work already enqueued on it,
+ *                    and work enqueued on it afterwards starts after the
+ *                    call's last copy; the host buffers must stay valid and
+ *                    unchanged until then.  The call returns after enqueuing
+ *                    (synchronise the stream before reading the outputs).
+ * Errors as for h3qk_prepare; a workspace that is too small is
+ * H3QK_ERR_INVALID_ARG.  Host calls on one device enqueue one at a time.
+ */
+size_t h3qk_host_workspace_bytes(int64_t tokens, int32_t heads, int32_t head_dim, h3qk_dtype out_dtype,
+                                 h3qk_scale_mode scale_mode, const h3qk_opts* opts);
+
+h3qk_status h3qk_prepare_host(const void* qkv, const float* norm_wq, const float* norm_wk,
+                              const int32_t* positions, int64_t tokens, int32_t heads, int32_t head_dim,
+                              int32_t rotary_dim, int64_t valid_len, h3qk_dtype out_dtype,
+                              h3qk_scale_mode scale_mode, void* out_q, void* out_k, void* out_v,
+                              float* out_scales, const h3qk_opts* opts, void* workspace,
+                              size_t workspace_bytes, h3qk_stream_t stream);
+
+/*
  * h3qk_prepare_noalloc: h3qk_prepare for callers that cannot allocate device
  * memory at the point of the call -- for example a plugin inside an inference
  * engine that receives all of its memory up front, or a real-time decode loop

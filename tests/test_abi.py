@@ -192,6 +192,53 @@ def test_sage_valid_call_without_a_device_reports_cuda_error():
     assert _sage() == h3qk.ERR_CUDA
 
 
+def _host(**kw):
+    o = h3qk.default_opts()
+    o.in_dtype = h3qk.BF16
+    for k in ("sat_counts", "workspace"):
+        if k in kw:
+            setattr(o, k, kw.pop(k))
+    a = dict(qkv=QKV, norm_wq=WQ, norm_wk=WK, positions=POS, tokens=N, heads=H, head_dim=D, rotary_dim=R,
+             valid_len=N, out_dtype=h3qk.BF16, scale_mode=h3qk.SCALE_NONE, out_q=OQ, out_k=OK_, out_v=OV,
+             out_scales=None, ws=A + 0x6000000, ws_bytes=1 << 30)
+    a.update(kw)
+    return h3qk.prepare_host_ptr(a["qkv"], a["norm_wq"], a["norm_wk"], a["positions"], a["tokens"], a["heads"],
+                                 a["head_dim"], a["rotary_dim"], a["valid_len"], a["out_dtype"], a["scale_mode"],
+                                 a["out_q"], a["out_k"], a["out_v"], a["out_scales"], o, a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(ws=None), h3qk.ERR_INVALID_ARG),
+    (dict(ws=A + 0x6000000 + 64), h3qk.ERR_MISALIGNED),
+    (dict(ws_bytes=1024), h3qk.ERR_INVALID_ARG),
+    (dict(sat_counts=SC), h3qk.ERR_INVALID_ARG),
+    (dict(workspace=WS), h3qk.ERR_INVALID_ARG),
+    (dict(head_dim=12), h3qk.ERR_INVALID_ARG),
+    (dict(out_dtype=h3qk.FP16), h3qk.ERR_INVALID_ARG),
+    (dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC), h3qk.ERR_INVALID_ARG),  # no out_scales
+    (dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_STATIC, out_scales=SC), h3qk.ERR_INVALID_ARG),  # no table
+    (dict(out_q=None), h3qk.ERR_INVALID_ARG),
+    (dict(valid_len=N + 1), h3qk.ERR_INVALID_ARG),
+])
+def test_host_entry_checks_arguments(kw, want):
+    assert _host(**kw) == want
+
+
+def test_host_entry_valid_call_without_a_device_reports_cuda_error():
+    assert _host() == h3qk.ERR_CUDA
+
+
+@pytest.mark.pure_host
+def test_host_workspace_bytes():
+    o = h3qk.default_opts()
+    small = h3qk.host_workspace_bytes(4896, 16, 64, h3qk.FP16, h3qk.SCALE_NONE, o)
+    big = h3qk.host_workspace_bytes(65280, 24, 128, h3qk.BF16, h3qk.SCALE_NONE, o)
+    dyn = h3qk.host_workspace_bytes(65280, 24, 128, h3qk.E4M3, h3qk.SCALE_DYNAMIC, o)
+    assert 0 < small < big < dyn
+    assert h3qk.host_workspace_bytes(10, 16, 64, h3qk.FP16, h3qk.SCALE_NONE, o) % 256 == 0
+    assert h3qk.host_workspace_bytes(-1, 16, 64, h3qk.FP16, h3qk.SCALE_NONE, o) == 0
+
+
 def _vae(fn, **kw):
     L = h3qk.lib()
     if fn == "silu":

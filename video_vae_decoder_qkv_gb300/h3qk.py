@@ -280,6 +280,92 @@ def prepare_sage(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int,
     return q, k, v
 
 
+def _host_sigs(L):
+    if L.h3qk_prepare_host.argtypes is None:
+        P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.h3qk_host_workspace_bytes.restype = ctypes.c_size_t
+        L.h3qk_host_workspace_bytes.argtypes = [I64, I32, I32, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Opts)]
+        L.h3qk_prepare_host.restype = ctypes.c_int
+        L.h3qk_prepare_host.argtypes = [P, P, P, P, I64, I32, I32, I32, I64, ctypes.c_int, ctypes.c_int, P, P, P, P,
+                                        ctypes.POINTER(Opts), P, ctypes.c_size_t, P]
+
+
+def host_workspace_bytes(tokens: int, heads: int, head_dim: int, out_dtype: int, scale_mode: int, opts=None) -> int:
+    L = lib()
+    _host_sigs(L)
+    return int(L.h3qk_host_workspace_bytes(tokens, heads, head_dim, out_dtype, scale_mode,
+                                           ctypes.byref(opts) if opts is not None else None))
+
+
+def prepare_host_ptr(qkv, norm_wq, norm_wk, positions, tokens, heads, head_dim, rotary_dim, valid_len, out_dtype,
+                     scale_mode, out_q, out_k, out_v, out_scales, opts, workspace, workspace_bytes, stream) -> int:
+    """h3qk_prepare_host on raw pointers (host buffers, device workspace); returns the status."""
+    L = lib()
+    _host_sigs(L)
+    return L.h3qk_prepare_host(qkv, norm_wq, norm_wk, positions, tokens, heads, head_dim, rotary_dim, valid_len,
+                               out_dtype, scale_mode, out_q, out_k, out_v, out_scales,
+                               ctypes.byref(opts) if opts is not None else None, workspace, workspace_bytes, stream)
+
+
+def prepare_host(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rotary_dim: int,
+                 batch: int = 1, valid_len: int | None = None, scale_mode: str = "none",
+                 n_axes: int | None = None, axis_dims=None, theta: float = 10000.0, eps: float = 1e-6,
+                 static_scales=None, out=None, out_scales=None, workspace=None, stream=None,
+                 out_layout: str = "head_major", valid_lens=None, device=None):
+    """The path on host (CPU) tensors, one library call: inputs are copied to
+    the GPU, computed and copied back in overlapping chunks.  Arguments as for
+    ``prepare``, but every tensor is a CPU tensor (pinned memory lets the
+    copies overlap); ``static_scales`` and ``valid_lens`` are CPU tensors too.
+    ``workspace`` is a CUDA uint8 tensor of ``host_workspace_bytes`` bytes
+    (allocated when None).  Returns (q, k, v, scales) as CPU tensors; they are
+    ready once ``stream`` (default: the current stream) has been
+    synchronised."""
+    import torch
+
+    if qkv.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("qkv must be float16 or bfloat16")
+    if qkv.device.type != "cpu":
+        raise ValueError("prepare_host takes host tensors")
+    tokens = qkv.shape[0]
+    if tokens % batch:
+        raise ValueError("tokens must be a multiple of batch")
+    seq = tokens // batch
+    if valid_len is None:
+        valid_len = seq
+    mode = _SCALE_NAMES[scale_mode]
+    in_dt = FP16 if qkv.dtype == torch.float16 else BF16
+    out_dt = in_dt if mode == SCALE_NONE else E4M3
+    if n_axes is None:
+        n_axes = positions.shape[1] if positions is not None and positions.dim() == 2 else 3
+    layout = {"head_major": HEAD_MAJOR, "token_major": TOKEN_MAJOR}[out_layout]
+    shape = (batch, heads, seq, head_dim) if layout == HEAD_MAJOR else (batch, seq, heads, head_dim)
+    if out is None:
+        tdt = qkv.dtype if out_dt != E4M3 else torch.uint8
+        out = tuple(torch.empty(shape, dtype=tdt).pin_memory() for _ in range(3))
+    q, k, v = out
+    if out_dt == E4M3 and out_scales is None:
+        out_scales = torch.empty(3, dtype=torch.float32).pin_memory()
+    o = _opts_for(qkv, n_axes=n_axes, axis_dims=axis_dims, theta=theta, eps=eps, batch=batch)
+    o.out_layout = layout
+    o.static_scales = _ptr(static_scales)
+    o.valid_lens = _ptr(valid_lens)
+    need = host_workspace_bytes(tokens, heads, head_dim, out_dt, mode, o)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    st = prepare_host_ptr(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens, heads,
+                          head_dim, rotary_dim, valid_len, out_dt, mode, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                          _ptr(out_scales) if out_dt == E4M3 else None, o, workspace.data_ptr(),
+                          workspace.numel() * workspace.element_size(), stream)
+    if st != OK:
+        raise H3QKError(st, status_string(st), int(lib().h3qk_last_cuda_error()))
+    return q, k, v, (out_scales if out_dt == E4M3 else None)
+
+
 def _opts_for(qkv, *, n_axes, axis_dims, theta, eps, batch):
     import torch
 
