@@ -13,24 +13,30 @@ import os
 import shutil
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libh3qk.so")
-SOURCES = [os.path.join(CSRC, "h3qk_api.cu"), os.path.join(CSRC, "h3qk_vae_ops.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "h3qk_kernels.cuh"), os.path.join(CSRC, "h3qk_internal.h"),
-                  os.path.join(INCLUDE, "h3qk.h")]
+# The kernel instances of each input type sit in their own translation unit
+# so that the sources compile in parallel.
+SOURCES = [os.path.join(CSRC, f) for f in ("h3qk_api.cu", "h3qk_launch_bf16.cu", "h3qk_launch_fp16.cu",
+                                           "h3qk_vae_ops.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("h3qk_kernels.cuh", "h3qk_launch.cuh", "h3qk_internal.h")] + \
+    [os.path.join(INCLUDE, "h3qk.h")]
 
-NVCC_FLAGS = [
-    "-O3", "-std=c++17", "--threads", "0",
+COMPILE_FLAGS = [
+    "-O3", "-std=c++17",
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-lineinfo",
     "-fmad=false", "-prec-div=true", "-prec-sqrt=true", "-ftz=false",
-    "-Xcompiler", "-fPIC", "-shared",
-    "-cudart", "static",
+    "-Xcompiler", "-fPIC",
 ]
+LINK_FLAGS = ["-shared", "-cudart", "static", "-gencode", "arch=compute_103a,code=sm_103a"]
+# One-shot form (all sources in one nvcc command), for tools that build variants.
+NVCC_FLAGS = COMPILE_FLAGS + ["--threads", "0", "-shared", "-cudart", "static"]
 
 
 def nvcc_path() -> str:
@@ -50,13 +56,30 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
     if not force and up_to_date():
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc_path(), *NVCC_FLAGS, *(extra or []), "-I", INCLUDE, "-I", CSRC, "-o", tmp, *SOURCES]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-        print(" ".join(cmd), flush=True)
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    tag = f".tmp{os.getpid()}"
+    objs = [os.path.join(PKG, os.path.basename(src) + tag + ".o") for src in SOURCES]
+
+    def compile_one(src_obj):
+        src, obj = src_obj
+        cmd = [nvcc_path(), *COMPILE_FLAGS, *(extra or []), "-I", INCLUDE, "-I", CSRC, "-c", "-o", obj, src]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if verbose or r.returncode:
+            sys.stdout.write(r.stdout)
+            sys.stderr.write(r.stderr)
+        r.check_returncode()
+
+    try:
+        with ThreadPoolExecutor(len(SOURCES)) as ex:
+            list(ex.map(compile_one, zip(SOURCES, objs)))
+        tmp = LIB + tag
+        subprocess.run([nvcc_path(), *LINK_FLAGS, "-o", tmp, *objs], check=True)
+        os.replace(tmp, LIB)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB
 
 

@@ -13,6 +13,17 @@
 #include "h3qk_internal.h"
 #include "h3qk_kernels.cuh"
 
+namespace h3qk {
+
+// Zero the three amax words of a dynamic call (defined here only: this is
+// the one translation unit that launches it).
+__global__ void amax_init_kernel(unsigned int* words)
+{
+    if (threadIdx.x < 3) words[threadIdx.x] = 0u;
+}
+
+}  // namespace h3qk
+
 namespace {
 
 thread_local int g_last_cuda_error = 0;
@@ -54,75 +65,11 @@ int next_pow2(int v)
     return p;
 }
 
-// One launch of a mode.  The grid covers the call's row groups (32/LPR
-// token rows per warp, 8 warps per block), capped at 8 blocks per SM; the
-// kernel grid-strides over the rest.  Modes with a shared-memory pipeline
-// take dynamic shared memory; the kernel's dynamic limit is raised to that
-// size once per device (static and dynamic together may exceed the 48 KB
-// default).
-template <bool BF16, int LPR, int CH, int MODE>
-cudaError_t launch_one(const h3qk::Params& p, cudaStream_t st)
-{
-    constexpr size_t smem = h3qk::stage_bytes<CH, MODE>();
-    auto* kernel = h3qk::qkprep_kernel<BF16, LPR, CH, MODE>;
-    if constexpr (smem > 0) {
-        static std::mutex mu;
-        static bool raised[kMaxDevices] = {false};
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
-        std::lock_guard<std::mutex> lock(mu);
-        if (!raised[dev]) {
-            const cudaError_t e =
-                cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-            if (e != cudaSuccess) return e;
-            raised[dev] = true;
-        }
-    }
-    constexpr int64_t tpw = 32 / LPR;
-    const int64_t groups = (p.rows + tpw - 1) / tpw;
-    const int64_t want = (groups + h3qk::kWarpsPerBlock - 1) / h3qk::kWarpsPerBlock;
-    const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
-    const int blocks = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
-    kernel<<<blocks, h3qk::kThreads, smem, st>>>(p);
-    ++g_launches;
-    return cudaGetLastError();
-}
-
-// P = next_pow2(D/8) chunk slots per head row: the mode's CH per lane on
-// P/CH lanes (fewer per lane when P < CH).
-template <bool BF16, int MODE>
-cudaError_t launch_p(int P, const h3qk::Params& p, cudaStream_t st)
-{
-    constexpr int CH = h3qk::Tune<MODE>::CH;
-    static_assert(CH == 1 || CH == 2 || CH == 4, "1, 2 or 4 chunks per lane");
-    if (P < CH) {
-        if (P == 1) return launch_one<BF16, 1, 1, MODE>(p, st);
-        return launch_one<BF16, 1, 2, MODE>(p, st);  // P == 2 < CH == 4
-    }
-    switch (P / CH) {
-    case 1: return launch_one<BF16, 1, CH, MODE>(p, st);
-    case 2: return launch_one<BF16, 2, CH, MODE>(p, st);
-    case 4: return launch_one<BF16, 4, CH, MODE>(p, st);
-    case 8: return launch_one<BF16, 8, CH, MODE>(p, st);
-    case 16: return launch_one<BF16, 16, CH, MODE>(p, st);
-    default: return launch_one<BF16, 32 / CH, CH, MODE>(p, st);
-    }
-}
-
-template <bool BF16>
-cudaError_t launch_m(int P, int mode, const h3qk::Params& p, cudaStream_t st)
-{
-    switch (mode) {
-    case h3qk::kOut16: return launch_p<BF16, h3qk::kOut16>(P, p, st);
-    case h3qk::kAmax: return launch_p<BF16, h3qk::kAmax>(P, p, st);
-    case h3qk::kSage: return launch_p<BF16, h3qk::kSage>(P, p, st);
-    default: return launch_p<BF16, h3qk::kCast>(P, p, st);
-    }
-}
-
+// The kernel launches live in one translation unit per input type
+// (h3qk_launch.cuh, compiled twice), so the build compiles them in parallel.
 cudaError_t launch(bool bf16, int P, int mode, const h3qk::Params& p, cudaStream_t st)
 {
-    return bf16 ? launch_m<true>(P, mode, p, st) : launch_m<false>(P, mode, p, st);
+    return bf16 ? h3qk_internal_launch_bf16(P, mode, p, st) : h3qk_internal_launch_fp16(P, mode, p, st);
 }
 
 h3qk_status fail_cuda(cudaError_t e)

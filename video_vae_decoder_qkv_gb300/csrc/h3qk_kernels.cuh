@@ -128,6 +128,8 @@ struct Params {
     unsigned int* sat_counts;    // cast mode: clipped-element counters (device), or null
     float kv_scale;              // sage mode: factor of K (binary32 out) and V (binary16 out)
     int64_t pf_span;             // elements of an input row the call reads ([0, pf_span))
+    int32_t hs_shift;            // sliced launches: log2 of the head slices per row group
+    int32_t hs_heads;            // sliced launches: heads per slice
     float inv_freq[kMaxPairs];   // per rotary pair
     uint8_t axis[kMaxPairs];     // position axis of each rotary pair
 };
@@ -489,7 +491,7 @@ __device__ __forceinline__ void emit_e4m3(const uint32_t (&y)[4], float f, uint8
 // tensor; kCast writes e4m3 codes under the dynamic or static factors; kSage
 // writes binary32 Q, binary32 K * kv_scale and binary16 V * kv_scale.
 // ---------------------------------------------------------------------------
-template <bool BF16, int LPR, int CH, int MODE>
+template <bool BF16, int LPR, int CH, int MODE, bool SLICED>
 __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const __grid_constant__ Params p)
 {
     static_assert(CH == 1 || CH == 2 || CH == 4, "1, 2 or 4 chunks per lane");
@@ -508,6 +510,11 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
     const int D = p.head_dim;
     const bool count_sat = MODE == kCast && p.sat_counts != nullptr;
     const int64_t n_groups = (p.rows + TPW - 1) / TPW;
+    // Work items: a row group, or (SLICED, for calls too small to fill the
+    // GPU) one of 2^hs_shift slices of hs_heads heads of a row group.
+    const int hs_shift = SLICED ? p.hs_shift : 0;
+    const int64_t n_items = n_groups << hs_shift;
+    const int hs_mask = (1 << hs_shift) - 1;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
 
@@ -575,12 +582,17 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
     extern __shared__ __align__(16) uint4 h3qk_stage[];
     uint4* const ring = h3qk_stage + static_cast<size_t>(threadIdx.x >> 5) * (S > 0 ? S * U * CH * 32 : 0);
     const int first_part = p.qk_first < p.qk_end ? p.qk_first : 2;
-    int64_t fg = warp0;          // issue cursor: group, part, first head, stage
-    int fpart = first_part, fh0 = 0, fstage = 0;
+    int64_t fit = warp0;         // issue cursor: work item, part, head, stage
+    int fpart = first_part, fh0 = 0, fh_lo = 0, fh_hi = H, fstage = 0;
     const uint16_t* frow = p.qkv;
     bool fact[CH];
-    auto feed_group = [&]() {    // row pointer and active chunks of group fg
-        const int64_t rr = fg * TPW + sub;
+    auto feed_group = [&]() {    // head slice, row pointer and active chunks of item fit
+        if constexpr (SLICED) {
+            fh_lo = static_cast<int>(fit & hs_mask) * p.hs_heads;
+            fh_hi = min(H, fh_lo + p.hs_heads);
+            fh0 = fh_lo;
+        }
+        const int64_t rr = (fit >> hs_shift) * TPW + sub;
         bool ok = false;
         if (rr < p.rows) {
             const int64_t bb = rr / p.seq;
@@ -597,26 +609,26 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
     };
     auto issue = [&]() {         // copies of the next batch, one commit group
         if constexpr (S > 0) {
-            if (fg < n_groups) {
+            if (fit < n_items) {
                 uint4* st = ring + fstage * (U * CH * 32);
 #pragma unroll
                 for (int u = 0; u < U; ++u)
 #pragma unroll
                     for (int q = 0; q < CH; ++q)
-                        if (fh0 + u < H && fact[q])
+                        if (fh0 + u < fh_hi && fact[q])
                             cp_async16(st + (u * CH + q) * 32 + lane,
                                        frow + p.in_part_off[fpart] + static_cast<int64_t>(fh0 + u) * D + 8 * q * LPR);
                 fh0 += U;
-                if (fh0 >= H) {
-                    fh0 = 0;
+                if (fh0 >= fh_hi) {
+                    fh0 = fh_lo;
                     if (fpart < 2 && fpart + 1 < p.qk_end) {
                         ++fpart;
                     } else if (fpart < 2 && p.has_v) {
                         fpart = 2;
                     } else {
                         fpart = first_part;
-                        fg += n_warps;
-                        if (fg < n_groups) feed_group();
+                        fit += n_warps;
+                        if (fit < n_items) feed_group();
                     }
                 }
             }
@@ -628,12 +640,15 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
     if constexpr (S > 0) {
 #pragma unroll
         for (int q = 0; q < CH; ++q) fact[q] = false;
-        if (fg < n_groups) feed_group();
+        if (fit < n_items) feed_group();
 #pragma unroll 1
         for (int k = 0; k < S - 1; ++k) issue();
     }
 
-    for (int64_t g = warp0; g < n_groups; g += n_warps) {
+    for (int64_t it = warp0; it < n_items; it += n_warps) {
+        const int64_t g = it >> hs_shift;
+        const int h_lo = SLICED ? static_cast<int>(it & hs_mask) * p.hs_heads : 0;
+        const int h_hi = SLICED ? min(H, h_lo + p.hs_heads) : H;
         const int64_t r = g * TPW + sub;
         int64_t b = 0, s = 0;
         bool act_row = false;
@@ -692,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
                 int64_t rr = r;
                 if (off >= p.pf_span) {
                     off -= p.pf_span;
-                    rr += n_warps * TPW;
+                    rr = ((it + n_warps) >> hs_shift) * TPW + sub;
                 }
                 if (rr >= p.rows || off >= p.pf_span) return;
                 if (off + n > p.pf_span) n = p.pf_span - off;
@@ -705,12 +720,12 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
         for (int part = 0; part < 2; ++part) {
             if (part < p.qk_first || part >= p.qk_end) continue;  // warp-uniform
             const uint16_t* src = rowp + p.in_part_off[part];
-            for (int h0 = 0; h0 < H; h0 += U) {
+            for (int h0 = h_lo; h0 < h_hi; h0 += U) {
                 prefetch(p.in_part_off[part] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(U) * D);
                 if constexpr (MODE == kAmax) {
                     // Once per part: re-reading every batch made the three amax
                     // words a hot spot for every warp of the grid.
-                    if (h0 == 0) {
+                    if (h0 == h_lo) {
                         const uint32_t gw = lane == 0 ? __ldcg(p.amax_words + p.slot[part]) : 0u;
                         thr[part] = __shfl_sync(0xffffffffu, gw, 0);
                     }
@@ -737,14 +752,14 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
 #pragma unroll
                         for (int q = 0; q < CH; ++q) {
                             raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
-                            if (h0 + u < H && act[q])
+                            if (h0 + u < h_hi && act[q])
                                 raw[u][q] = load16(src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR);
                         }
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int h = h0 + u;
-                    if (h >= H) break;  // warp-uniform
+                    if (h >= h_hi) break;  // warp-uniform
                     uint4 rw[CH];
 #pragma unroll
                     for (int q = 0; q < CH; ++q) rw[q] = raw[u][q];
@@ -808,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
         // ---- V: passed through ----------------------------------------------
         if (p.has_v) {
             const uint16_t* src = rowp + p.in_part_off[2];
-            for (int h0 = 0; h0 < H; h0 += UV) {
+            for (int h0 = h_lo; h0 < h_hi; h0 += UV) {
                 prefetch(p.in_part_off[2] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(UV) * D);
                 uint4 raw[UV][CH];
                 if constexpr (S > 0) {
@@ -827,14 +842,14 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
 #pragma unroll
                         for (int q = 0; q < CH; ++q) {
                             raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
-                            if (h0 + u < H && act[q])
+                            if (h0 + u < h_hi && act[q])
                                 raw[u][q] = load16(src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR);
                         }
                 }
 #pragma unroll
                 for (int u = 0; u < UV; ++u) {
                     const int h = h0 + u;
-                    if (h >= H) break;  // warp-uniform
+                    if (h >= h_hi) break;  // warp-uniform
 #pragma unroll
                     for (int q = 0; q < CH; ++q) {
                         if (!act[q]) continue;
@@ -894,10 +909,5 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
     }
 }
 
-// Zero the three amax words of a dynamic call.
-__global__ void amax_init_kernel(unsigned int* words)
-{
-    if (threadIdx.x < 3) words[threadIdx.x] = 0u;
-}
 
 }  // namespace h3qk

@@ -1,0 +1,116 @@
+// Kernel launches of one input type (BF16 true or false): the mode's lane
+// layout, the plain or head-sliced kernel, and the grid.  Included by
+// h3qk_launch_bf16.cu and h3qk_launch_fp16.cu, one instance set each.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "h3qk_internal.h"
+#include "h3qk_kernels.cuh"
+
+namespace h3qk_launch {
+// Internal linkage on purpose: function-local statics of templates with
+// external linkage become process-wide unique symbols, which the dynamic
+// linker would share with any other copy of this library in the process
+// (one copy would then skip raising the shared memory limit of its own
+// kernels).
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// One launch of a mode.  The grid covers the call's row groups (32/LPR
+// token rows per warp, 8 warps per block), capped at 8 blocks per SM; the
+// kernel grid-strides over the rest.  Modes with a shared-memory pipeline
+// take dynamic shared memory; the kernel's dynamic limit is raised to that
+// size once per device (static and dynamic together may exceed the 48 KB
+// default).
+template <bool BF16, int LPR, int CH, int MODE, bool SLICED>
+cudaError_t launch_sliced(const h3qk::Params& p, cudaStream_t st)
+{
+    constexpr size_t smem = h3qk::stage_bytes<CH, MODE>();
+    auto* kernel = h3qk::qkprep_kernel<BF16, LPR, CH, MODE, SLICED>;
+    if constexpr (smem > 0) {
+        static std::mutex mu;
+        static bool raised[kMaxDevices] = {false};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!raised[dev]) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+            raised[dev] = true;
+        }
+    }
+    constexpr int64_t tpw = 32 / LPR;
+    const int64_t groups = ((p.rows + tpw - 1) / tpw) << (SLICED ? p.hs_shift : 0);
+    const int64_t want = (groups + h3qk::kWarpsPerBlock - 1) / h3qk::kWarpsPerBlock;
+    const int64_t cap = static_cast<int64_t>(h3qk_internal_sm_count()) * 8;
+    const int blocks = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
+    kernel<<<blocks, h3qk::kThreads, smem, st>>>(p);
+    h3qk_internal_count_launch();
+    return cudaGetLastError();
+}
+
+// A call whose row groups would fill fewer than about 16 warps per SM splits
+// each group's heads into 2^shift slices of at least 2 heads (no slice
+// empty: the copy pipeline walks one batch sequence per slice and part) and
+// runs the sliced kernel; every other call runs the plain kernel.
+template <bool BF16, int LPR, int CH, int MODE>
+cudaError_t launch_one(const h3qk::Params& p0, cudaStream_t st)
+{
+    constexpr int64_t tpw = 32 / LPR;
+    const int64_t groups = (p0.rows + tpw - 1) / tpw;
+    const int64_t target = static_cast<int64_t>(h3qk_internal_sm_count()) * 16;
+    const int heads = p0.heads;
+    int shift = 0;
+    while (shift < 4 && (groups << shift) < target && (heads + (2 << shift) - 1) / (2 << shift) >= 2) ++shift;
+    int per = (heads + (1 << shift) - 1) >> shift;
+    while (shift > 0 && ((1 << shift) - 1) * per >= heads) {
+        --shift;
+        per = (heads + (1 << shift) - 1) >> shift;
+    }
+    if (shift == 0) return launch_sliced<BF16, LPR, CH, MODE, false>(p0, st);
+    h3qk::Params p = p0;
+    p.hs_shift = shift;
+    p.hs_heads = per;
+    return launch_sliced<BF16, LPR, CH, MODE, true>(p, st);
+}
+
+// P = next_pow2(D/8) chunk slots per head row: the mode's CH per lane on
+// P/CH lanes (fewer per lane when P < CH).
+template <bool BF16, int MODE>
+cudaError_t launch_p(int P, const h3qk::Params& p, cudaStream_t st)
+{
+    constexpr int CH = h3qk::Tune<MODE>::CH;
+    static_assert(CH == 1 || CH == 2 || CH == 4, "1, 2 or 4 chunks per lane");
+    if (P < CH) {
+        if (P == 1) return launch_one<BF16, 1, 1, MODE>(p, st);
+        return launch_one<BF16, 1, 2, MODE>(p, st);  // P == 2 < CH == 4
+    }
+    switch (P / CH) {
+    case 1: return launch_one<BF16, 1, CH, MODE>(p, st);
+    case 2: return launch_one<BF16, 2, CH, MODE>(p, st);
+    case 4: return launch_one<BF16, 4, CH, MODE>(p, st);
+    case 8: return launch_one<BF16, 8, CH, MODE>(p, st);
+    case 16: return launch_one<BF16, 16, CH, MODE>(p, st);
+    default: return launch_one<BF16, 32 / CH, CH, MODE>(p, st);
+    }
+}
+
+template <bool BF16>
+cudaError_t launch_m(int P, int mode, const h3qk::Params& p, cudaStream_t st)
+{
+    switch (mode) {
+    case h3qk::kOut16: return launch_p<BF16, h3qk::kOut16>(P, p, st);
+    case h3qk::kAmax: return launch_p<BF16, h3qk::kAmax>(P, p, st);
+    case h3qk::kSage: return launch_p<BF16, h3qk::kSage>(P, p, st);
+    default: return launch_p<BF16, h3qk::kCast>(P, p, st);
+    }
+}
+
+
+}  // namespace
+}  // namespace h3qk_launch

@@ -1,0 +1,7 @@
+// Kernel instances and launches for binary16 inputs.
+#include "h3qk_launch.cuh"
+
+cudaError_t h3qk_internal_launch_fp16(int P, int mode, const h3qk::Params& p, cudaStream_t st)
+{
+    return h3qk_launch::launch_m<false>(P, mode, p, st);
+}
