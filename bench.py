@@ -27,7 +27,6 @@ import os
 import statistics
 import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -39,7 +38,7 @@ METRIC = "fused QK-prep HBM GB/s and % of GB300 peak; tokens/s at 65k-token tile
 SPEC16 = W.LATENT_65K
 SPEC8 = W.LATENT_65K_E4M3
 KERNEL_FILES = ["video_vae_decoder_qkv_gb300/csrc/h3qk_kernels.cuh",
-                "video_vae_decoder_qkv_gb300/csrc/h3qk_api.cu"]
+                "video_vae_decoder_qkv_gb300/csrc/h3qk_launch.cuh"]
 WORKLOAD = ("latent_65k: 544x960 latent grid T32xH34xW60 = 65,280 tokens, 24 heads x 128, "
             "rotary 96 (32/32/32 over t,h,w), BF16 packed QKV ~N(0,1) with 0.1% x50 outlier "
             "columns; each step: BF16 head-major out, then e4m3 out with dynamic scales")
@@ -112,15 +111,13 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = None
 
     def start(self):
+        # samples arrive on a pipe (no file is written)
         try:
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
-            os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             time.sleep(0.3)
         except OSError:
             self.proc = None
@@ -131,16 +128,15 @@ class ClockSampler:
         time.sleep(0.1)
         self.proc.terminate()
         try:
-            self.proc.wait(timeout=5)
+            text, _ = self.proc.communicate(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+            text, _ = self.proc.communicate()
         rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        os.unlink(self.path)
+        for line in (text or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
         if not rows:
             return None
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -334,6 +330,61 @@ def variant_ops(dev, stream, qkv, wq, wk, pos, common, spec, iters: int = 20):
     return rows
 
 
+def small_calls(dev, calls: int = 50):
+    """The decoder tile (4,896 tokens, 16 x 64, fp16 out) and the batch of 8
+    such tiles (e4m3 dynamic): per-call GPU time from `calls` calls captured
+    in one CUDA graph and replayed, which leaves out the Python and launch
+    overhead that dominates an event pair around one call this small."""
+    import numpy as np
+    import torch
+
+    from video_vae_decoder_qkv_gb300 import prepare
+
+    rows = {}
+    for spec in (W.DECODER_TILE, W.BATCHED_FP8):
+        inp = W.generate(spec)
+        dt = torch.float16 if spec.in_dtype == W.FP16 else torch.bfloat16
+        qkv = torch.from_numpy(inp.qkv.view(np.int16)).to(dev).view(dt)
+        wq, wk, pos = (torch.from_numpy(a).to(dev) for a in (inp.wq, inp.wk, inp.pos))
+        mode = {W.SCALE_NONE: "none", W.SCALE_DYNAMIC: "dynamic", W.SCALE_STATIC: "static"}[spec.scale_mode]
+        shape = (spec.batch, spec.heads, spec.seq, spec.head_dim)
+        odt = torch.float8_e4m3fn if spec.out_kind == W.OUT_E4M3 else dt
+        out = tuple(torch.empty(shape, dtype=odt, device=dev) for _ in range(3))
+        sc = torch.empty(3, device=dev)
+        ws = torch.zeros(4, dtype=torch.int32, device=dev)
+        side = torch.cuda.Stream(dev)
+        kw = dict(heads=spec.heads, head_dim=spec.head_dim, rotary_dim=spec.rotary_dim, batch=spec.batch,
+                  valid_len=spec.valid_len, scale_mode=mode, n_axes=spec.n_axes, axis_dims=spec.axis_dims,
+                  out=out, out_scales=sc, workspace=ws, stream=side)
+        try:
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    prepare(qkv, wq, wk, pos, **kw)
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(calls):
+                    prepare(qkv, wq, wk, pos, **kw)
+            ts = []
+            for _ in range(10):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                b.synchronize()
+                ts.append(a.elapsed_time(b) / calls)
+            ms = statistics.median(ts)
+            rows[spec.name] = {"us_per_call": 1e3 * ms, "GB/s": spec.algorithmic_bytes() / (ms / 1e3) / 1e9,
+                               "bytes": spec.algorithmic_bytes(), "tokens": spec.rows,
+                               "mode": "fp16 out" if mode == "none" else f"e4m3 {mode}"}
+            del g
+        except Exception as e:  # noqa: BLE001 - report, do not fail the bench line
+            rows[spec.name] = {"error": str(e)[:200]}
+        del qkv, out
+        torch.cuda.empty_cache()
+    return rows
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -448,6 +499,7 @@ def run_ours(args):
 
     variants = variant_ops(dev, stream, qkv, wq, wk, pos, common, spec16)
     extra = adjacent_ops(dev, stream) if not args.tokens else None
+    small = small_calls(dev) if not args.tokens else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.tokens:
@@ -489,6 +541,7 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h, "steps": E, "api": "h3qk_prepare_host (host buffers, chunked copies overlapped with the kernels), both calls of the step"},
             "gpu_launches": launches,
             "variants": variants,
+            "small_calls": small,
             "adjacent_ops": extra,
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -43,6 +43,26 @@ def test_every_declared_symbol_is_exported(L):
 
 
 @pytest.mark.pure_host
+def test_only_the_c_abi_is_exported(L):
+    """The library exports its C-ABI and nothing a second copy of it in the
+    same process could bind to: no process-wide unique objects (the dynamic
+    linker shares those across copies) and no other functions."""
+    import shutil
+    import subprocess
+
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", h3qk.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout.split("\n")
+    syms = [line.split() for line in out if line.strip()]
+    unique = [s for s in syms if len(s) == 3 and s[1] == "u"]
+    assert not unique, unique[:5]
+    funcs = {s[2] for s in syms if len(s) == 3 and s[1] == "T"}
+    assert funcs == set(h3qk.declared_functions()), sorted(funcs ^ set(h3qk.declared_functions()))
+
+
+@pytest.mark.pure_host
 def test_opts_layout_and_defaults(L):
     o = h3qk.default_opts()
     assert ctypes.sizeof(h3qk.Opts) == 96
