@@ -433,28 +433,54 @@ __device__ __forceinline__ void store_v_f16(const uint4& raw, float k, uint16_t*
 // differ by a subnormal quantum, a large relative error when the whole sum is
 // a few quanta (and a rotated pair of such a row reaches ordinary sizes).
 // Above 2^-96 those absolute differences are below 2^-40 relative.
+// bfloat16 inputs accumulate their squares as packed bfloat16 fused
+// multiply-adds on the input words (no widening): each of the 4*CH steps per
+// half rounds up by at most 2^-8 relative, so the sum is at most
+// (1 + 2^-8)^(4 CH) above the exact one (below it is the safe side), inv at
+// most (1 + 2^-8)^(2 CH) below, and the constant grows to 1.47 for CH = 2
+// (1.45 for CH = 1, 1.49 for CH = 4), again with about 1.5 % to spare.  An
+// overflowing or vanishing packed sum meets the two guards above.
 template <bool BF16, int LPR, int CH>
 __device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, float inv_d, float eps, int D)
 {
     uint32_t m2 = 0u;
-    float2 acc = make_float2(0.0f, 0.0f);
+    float ss;
+    if constexpr (BF16) {
+        uint32_t acc = 0u;  // two bfloat16 partial sums
 #pragma unroll
-    for (int q = 0; q < CH; ++q)
+        for (int q = 0; q < CH; ++q)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t w = word(raw[q], i);
-            m2 = hmax2_abs<BF16>(m2, w);
-            const float2 x = widen2<BF16>(w);
-            acc = __ffma2_rn(x, x, acc);
-        }
-    float ss = acc.x + acc.y;
+            for (int i = 0; i < 4; ++i) {
+                uint32_t w = word(raw[q], i);
+                m2 = hmax2_abs<true>(m2, w);
+                __nv_bfloat162 r = __hfma2(*reinterpret_cast<__nv_bfloat162*>(&w),
+                                           *reinterpret_cast<__nv_bfloat162*>(&w),
+                                           *reinterpret_cast<__nv_bfloat162*>(&acc));
+                acc = *reinterpret_cast<uint32_t*>(&r);
+            }
+        const float2 a = widen2<true>(acc);
+        ss = a.x + a.y;
+    } else {
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int q = 0; q < CH; ++q)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t w = word(raw[q], i);
+                m2 = hmax2_abs<false>(m2, w);
+                const float2 x = widen2<false>(w);
+                acc = __ffma2_rn(x, x, acc);
+            }
+        ss = acc.x + acc.y;
+    }
 #pragma unroll
     for (int o = LPR / 2; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (!(ss < 0x1p126f)) return __int_as_float(0x7f800000);  // +inf: never skip
     const float t = ss * (inv_d != 0.0f ? inv_d : 1.0f / static_cast<float>(D)) + eps;
     if (!(t >= 0x1p-96f)) return __int_as_float(0x7f800000);  // +inf: never skip
     const float inv = rsqrtf(t);
-    return 1.45f * inv * hmax2_to_float<BF16>(m2) * wmax + 0x1p-23f;
+    constexpr float kMargin = !BF16 ? 1.45f : (CH == 1 ? 1.45f : (CH == 2 ? 1.47f : 1.49f));
+    return kMargin * inv * hmax2_to_float<BF16>(m2) * wmax + 0x1p-23f;
 }
 
 // Eight 16-bit values -> eight e4m3 codes at dst (8 bytes); with COUNT, adds
