@@ -10,6 +10,21 @@
 #include "h3qk_internal.h"
 #include "h3qk_kernels.cuh"
 
+// Grid size per mode: 0 = up to 8 blocks per SM (the kernel grid-strides over
+// the rest); k > 0 = k whole waves of the blocks that fit on an SM at once.
+#ifndef H3QK_WAVES_OUT16
+#define H3QK_WAVES_OUT16 0
+#endif
+#ifndef H3QK_WAVES_AMAX
+#define H3QK_WAVES_AMAX 1
+#endif
+#ifndef H3QK_WAVES_CAST
+#define H3QK_WAVES_CAST 4
+#endif
+#ifndef H3QK_WAVES_SAGE
+#define H3QK_WAVES_SAGE 0
+#endif
+
 namespace h3qk_launch {
 // Internal linkage on purpose: function-local statics of templates with
 // external linkage become process-wide unique symbols, which the dynamic
@@ -19,6 +34,14 @@ namespace h3qk_launch {
 namespace {
 
 constexpr int kMaxDevices = 64;
+
+template <int MODE>
+constexpr int waves()
+{
+    return MODE == h3qk::kOut16 ? H3QK_WAVES_OUT16
+                                : (MODE == h3qk::kAmax ? H3QK_WAVES_AMAX
+                                                       : (MODE == h3qk::kCast ? H3QK_WAVES_CAST : H3QK_WAVES_SAGE));
+}
 
 // One launch of a mode.  The grid covers the call's row groups (32/LPR
 // token rows per warp, 8 warps per block), capped at 8 blocks per SM; the
@@ -47,7 +70,20 @@ cudaError_t launch_sliced(const h3qk::Params& p, cudaStream_t st)
     constexpr int64_t tpw = 32 / LPR;
     const int64_t groups = ((p.rows + tpw - 1) / tpw) << (SLICED ? p.hs_shift : 0);
     const int64_t want = (groups + h3qk::kWarpsPerBlock - 1) / h3qk::kWarpsPerBlock;
-    const int64_t cap = static_cast<int64_t>(h3qk_internal_sm_count()) * 8;
+    int64_t cap = static_cast<int64_t>(h3qk_internal_sm_count()) * 8;
+    if constexpr (waves<MODE>() > 0) {
+        // A whole number of waves of the blocks that fit on an SM at once.
+        static int occ[kMaxDevices] = {0};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+        if (occ[dev] == 0) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, h3qk::kThreads, smem) != cudaSuccess || n < 1)
+                n = 1;
+            occ[dev] = n;
+        }
+        cap = static_cast<int64_t>(h3qk_internal_sm_count()) * occ[dev] * waves<MODE>();
+    }
     const int blocks = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
     kernel<<<blocks, h3qk::kThreads, smem, st>>>(p);
     h3qk_internal_count_launch();
