@@ -12,6 +12,9 @@
 
 // Grid size per mode: 0 = up to 8 blocks per SM (the kernel grid-strides over
 // the rest); k > 0 = k whole waves of the blocks that fit on an SM at once.
+#ifndef H3QK_BLOCKS_PER_SM
+#define H3QK_BLOCKS_PER_SM 8
+#endif
 #ifndef H3QK_WAVES_OUT16
 #define H3QK_WAVES_OUT16 0
 #endif
@@ -70,7 +73,7 @@ cudaError_t launch_sliced(const h3qk::Params& p, cudaStream_t st)
     constexpr int64_t tpw = 32 / LPR;
     const int64_t groups = ((p.rows + tpw - 1) / tpw) << (SLICED ? p.hs_shift : 0);
     const int64_t want = (groups + h3qk::kWarpsPerBlock - 1) / h3qk::kWarpsPerBlock;
-    int64_t cap = static_cast<int64_t>(h3qk_internal_sm_count()) * 8;
+    int64_t cap = static_cast<int64_t>(h3qk_internal_sm_count()) * H3QK_BLOCKS_PER_SM;
     if constexpr (waves<MODE>() > 0) {
         // A whole number of waves of the blocks that fit on an SM at once.
         static int occ[kMaxDevices] = {0};
