@@ -22,8 +22,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libh3qk.so")
 # The kernel instances of each input type sit in their own translation unit
 # so that the sources compile in parallel.
-SOURCES = [os.path.join(CSRC, f) for f in ("h3qk_api.cu", "h3qk_launch_bf16.cu", "h3qk_launch_fp16.cu",
-                                           "h3qk_vae_ops.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("h3qk_api.cu", "h3qk_host.cu", "h3qk_launch_bf16.cu",
+                                           "h3qk_launch_fp16.cu", "h3qk_vae_ops.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("h3qk_kernels.cuh", "h3qk_launch.cuh", "h3qk_internal.h")] + \
     [os.path.join(INCLUDE, "h3qk.h")]
 
