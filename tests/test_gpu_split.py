@@ -73,30 +73,49 @@ def test_row_shards_with_combined_amax_equal_one_call():
     assert np.array_equal(scales[0], scales[1]) and np.array_equal(scales[0], want[3].cpu().numpy())
 
 
-@pytest.mark.parametrize("pattern", ["late_max", "rising", "falling", "near_tie", "uniform"])
+# Head geometries: 4 token rows per warp (first bound only), 8 and 16 (first
+# bound, then the pairwise one).
+GEOMETRIES = {"d128": dict(heads=24, head_dim=128, rotary_dim=96, axis_dims=(32, 32, 32)),
+              "d64": dict(heads=16, head_dim=64, rotary_dim=48, axis_dims=(16, 16, 16)),
+              "d32": dict(heads=8, head_dim=32, rotary_dim=24, axis_dims=(8, 8, 8))}
+
+
+@pytest.mark.parametrize("geometry", list(GEOMETRIES))
+@pytest.mark.parametrize("pattern", ["late_max", "rising", "falling", "near_tie", "pair_tie", "uniform"])
 @pytest.mark.parametrize("dtype", [W.FP16, W.BF16])
-def test_amax_early_out_is_exact(pattern, dtype):
+def test_amax_early_out_is_exact(pattern, dtype, geometry):
     """The amax pass skips rows whose bound cannot exceed the running max;
     adversarial orders of magnitudes must still give the exact amax."""
     import torch
 
     spec = W.LATENT_65K.with_(name="eo", batch=2, seq=257, grid=(1, 1, 257), valid_len=250, in_dtype=dtype,
-                              out_kind=W.OUT_E4M3, scale_mode=W.SCALE_DYNAMIC)
+                              out_kind=W.OUT_E4M3, scale_mode=W.SCALE_DYNAMIC, **GEOMETRIES[geometry])
     inp = G.inputs(spec)
     vals = (inp.qkv.view(np.float16).astype(np.float32) if dtype == W.FP16
             else (inp.qkv.astype(np.uint32) << 16).view(np.float32)).copy()
     rows = spec.rows
     HD = spec.hd
+    D, R = spec.head_dim, spec.rotary_dim
     if pattern == "late_max":
-        vals[1 * spec.seq + 249, 5 * 128 + 17] = 900.0          # last valid row of item 1, Q head 5
-        vals[0 * spec.seq + 249, HD + 7 * 128 + 100] = -700.0    # K, pass-through channel
+        vals[1 * spec.seq + 249, 5 * D + 17] = 900.0            # last valid row of item 1, Q head 5
+        vals[0 * spec.seq + 249, HD + 7 * D + R + 4] = -700.0   # K, pass-through channel
     elif pattern == "rising":
         vals *= np.linspace(0.05, 3.0, rows, dtype=np.float32)[:, None]
     elif pattern == "falling":
         vals *= np.linspace(3.0, 0.05, rows, dtype=np.float32)[:, None]
     elif pattern == "near_tie":
         vals[:, :] = np.float32(1.0)
-        vals[137, 3 * 128 + 5] = np.float32(1.0078125)
+        vals[137, 3 * D + 5] = np.float32(1.0078125)
+    elif pattern == "pair_tie":
+        # flat rows, and in scattered rows one rotated pair (both channels)
+        # and one pass-through channel a step above: the pairwise bounds of
+        # those rows sit within a rounding of the running max
+        vals[:, :] = np.float32(1.0)
+        for r, h, j in ((31, 2, 6), (137, 3, 2), (249, 1, 10), (300, 4, R + 2)):
+            vals[r, h * D + j] = np.float32(1.0078125)
+            if j < R:
+                vals[r, h * D + j + 1] = np.float32(1.0078125)
+            vals[r, HD + h * D + j] = np.float32(1.0078125)
     conv = oracle.f32_to_f16 if dtype == W.FP16 else oracle.f32_to_bf16
     qkv = conv(vals).reshape(inp.qkv.shape)
     mod = W.Inputs(spec, qkv, inp.wq, inp.wk, inp.pos, inp.static_scales)

@@ -440,8 +440,11 @@ __device__ __forceinline__ void store_v_f16(const uint4& raw, float k, uint16_t*
 // most (1 + 2^-8)^(2 CH) below, and the constant grows to 1.47 for CH = 2
 // (1.45 for CH = 1, 1.49 for CH = 4), again with about 1.5 % to spare.  An
 // overflowing or vanishing packed sum meets the two guards above.
+// The sum under the root that the bound used goes to `t` (left unset when
+// the bound is infinite).
 template <bool BF16, int LPR, int CH>
-__device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, float inv_d, float eps, int D)
+__device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, float inv_d, float eps, int D,
+                                          float& t_out)
 {
     uint32_t m2 = 0u;
     float ss;
@@ -478,9 +481,59 @@ __device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, fl
     if (!(ss < 0x1p126f)) return __int_as_float(0x7f800000);  // +inf: never skip
     const float t = ss * (inv_d != 0.0f ? inv_d : 1.0f / static_cast<float>(D)) + eps;
     if (!(t >= 0x1p-96f)) return __int_as_float(0x7f800000);  // +inf: never skip
+    t_out = t;
     const float inv = rsqrtf(t);
     constexpr float kMargin = !BF16 ? 1.45f : (CH == 1 ? 1.45f : (CH == 2 ? 1.47f : 1.49f));
     return kMargin * inv * hmax2_to_float<BF16>(m2) * wmax + 0x1p-23f;
+}
+
+// Second, tighter test of the early-out, for rows whose first bound did not
+// allow a skip: true when some |y| of this lane's row slice may exceed
+// `known` (an exact |y| already seen).  With z_j = x_j w_j, every output of
+// a channel pair (j, j+1) obeys
+//   |y| <= (1 + u)^2 (1 + 2^-24)^4 sqrt(1 + 7e-7) inv sqrt(z_j^2 + z_{j+1}^2) + 3 a
+// (u = 2^-8 for bfloat16, 2^-11 for float16; a = half the 16-bit subnormal
+// step): the same steps as above with the rotation bounded by the pair's own
+// norm instead of sqrt(2) max|x| max|w| (a pair that is not rotated keeps one
+// of its two values, below the norm as well).  Squared and compared with
+// t = ss/D + eps from the first bound, no root or division is taken: skip
+// when K2 max_j(z_j^2 + z_{j+1}^2) <= known^2 t.  K2 covers (1 + u)^4, the
+// sine/cosine term, the binary32 steps on both sides (below 2^-16 together),
+// the approximate sum in t (bfloat16: up to (1 + 2^-8)^(4 CH) above the
+// exact one; float16: under 2^-19), and (1 + 2^-9)^2, which absorbs the
+// absolute term once known >= 2^-13 (3a <= 2^-23 <= 2^-10 known).  That gives
+// 1.0359, 1.0522 and 1.0856 for bfloat16 with CH = 1, 2, 4 and 1.0059 for
+// float16, taken as 1.04, 1.06, 1.09 and 1.01.  known above 2^60 (its
+// square could overflow) or below 2^-13 never allows a skip.  Nor does a
+// NaN or infinite pair square (from a NaN or infinite weight; the inputs are
+// finite once the first bound is): the maximum keeps a NaN, and the
+// comparison is then false.  An overflowing right-hand side is safe: its
+// exact value then exceeds every finite left-hand side.
+__device__ __forceinline__ float fmax_keep_nan(float a, float b)
+{
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+template <bool BF16, int CH>
+__device__ __forceinline__ bool qk_pair_may_exceed(const uint4 (&raw)[CH], const float4* w, float t, float known)
+{
+    float m = 0.0f;
+#pragma unroll
+    for (int q = 0; q < CH; ++q) {
+        const float4 wa = w[2 * q], wb = w[2 * q + 1];
+        const float wq[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 z = mul2(widen2<BF16>(word(raw[q], i)), make_float2(wq[2 * i], wq[2 * i + 1]));
+            m = fmax_keep_nan(m, __fmaf_rn(z.x, z.x, __fmul_rn(z.y, z.y)));
+        }
+    }
+    if (!(known >= 0x1p-13f && known <= 0x1p60f)) return true;
+    constexpr float kK2 = !BF16 ? 1.01f : (CH == 1 ? 1.04f : (CH == 2 ? 1.06f : 1.09f));
+    const float lhs = kK2 * m;
+    return !(lhs < 0x1p127f && lhs <= known * known * t);
 }
 
 // Eight 16-bit values -> eight e4m3 codes at dst (8 bytes); with COUNT, adds
@@ -793,10 +846,23 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
                         // Exact early-out: when no lane's bound exceeds the largest
                         // exact |y| known (this warp's, or the grid's published
                         // one), the row cannot raise the amax.
-                        const float bnd = qk_bound<BF16, LPR, CH>(rw, wmax[part], p.inv_d, p.eps, D);
+                        float t = 0.0f;
+                        const float bnd = qk_bound<BF16, LPR, CH>(rw, wmax[part], p.inv_d, p.eps, D, t);
                         const uint32_t bb = act_row ? __float_as_uint(bnd) : 0u;
                         const uint32_t known = run[part] > thr[part] ? run[part] : thr[part];
                         if (__reduce_max_sync(0xffffffffu, bb) <= known) continue;  // warp-uniform
+                        if constexpr (TPW >= 8) {
+                            // The vote spans 8 or more token rows here, so the
+                            // first bound fails often (about half the Q head rows
+                            // at head_dim 64), and the pairwise test pays for
+                            // itself; with 4 rows per warp it costs more than it
+                            // saves.
+                            const bool may = act_row && (!(bnd < 0x1p127f) ||
+                                                         qk_pair_may_exceed<BF16, CH>(
+                                                             rw, reinterpret_cast<const float4*>(&ws[part][c][0]), t,
+                                                             __uint_as_float(known)));
+                            if (!__any_sync(0xffffffffu, may)) continue;  // warp-uniform
+                        }
                         if (!have_angles) {
                             angles();
                             have_angles = true;
