@@ -509,6 +509,11 @@ def run_ours(args):
         cpu = {"value": b / s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"all {rows} tokens of the tile once, BF16 out then e4m3 dynamic, {threads} threads",
                "seconds": s}
+        # the same oracle on one thread (row ranges do not change its bytes)
+        rows1 = min(N, 4096)
+        s1, b1 = oracle_rows(inp, rows1, 1)
+        cpu["single_thread"] = {"value": b1 / s1 / 1e9, "unit": "GB/s", "cores": 1, "seconds": s1,
+                                "sample": f"first {rows1} tokens of the tile, BF16 out then e4m3 dynamic"}
 
     if rank == 0:
         peak, peak_src = measured_peak()
