@@ -31,8 +31,7 @@
 namespace h3qk {
 
 constexpr int kMaxPairs = 128;       // rotary_dim <= 256
-constexpr int kWarpsPerBlock = 8;
-constexpr int kThreads = 32 * kWarpsPerBlock;
+constexpr int kWarpsPerBlock = 8;    // head_dim > 64; see Shape for head_dim <= 64
 // Tuning knobs (compile-time; the defaults are the measured best):
 // H3QK_CH_<MODE> chunks of 8 channels per lane (1, 2 or 4; default H3QK_CH),
 // and per mode a five-digit code "U UV MIN_BLOCKS PF S": Q/K head rows per batch of
@@ -87,12 +86,48 @@ template <> struct Tune<kAmax> : TuneT<H3QK_TUNE_AMAX, H3QK_CH_AMAX> {};
 template <> struct Tune<kCast> : TuneT<H3QK_TUNE_CAST, H3QK_CH_CAST> {};
 template <> struct Tune<kSage> : TuneT<H3QK_TUNE_SAGE, H3QK_CH_SAGE> {};
 
-// Dynamic shared memory of one block of a mode: S stages x U head rows x CH
-// chunks x 32 lanes x 16 bytes per warp.
-template <int CH, int MODE>
+// Block shape of the instances whose warps hold 8 or more token rows (LPR <= 4,
+// head_dim <= 64), per mode as a code "W MB": warps per block (1 or 2 digits)
+// and the resident blocks per SM asked of the register allocator.  Their
+// per-row work (the reduction, the root and reciprocal, the angles) weighs
+// twice as much per byte as at head_dim 128.  Measured best: 16-bit output
+// in blocks of 10 warps, 2 per SM (20 warps of up to 96 registers, against
+// 8 x 2); amax and cast in blocks of 5 warps, 4 per SM (20 warps of up to 96
+// registers, against 24 warps of 80 that spill).  The larger heads keep
+// 8 warps per block and the MIN_BLOCKS digit of their tuning code.
+#ifndef H3QK_SMALL_OUT16
+#define H3QK_SMALL_OUT16 102
+#endif
+#ifndef H3QK_SMALL_AMAX
+#define H3QK_SMALL_AMAX 54
+#endif
+#ifndef H3QK_SMALL_CAST
+#define H3QK_SMALL_CAST 54
+#endif
+#ifndef H3QK_SMALL_SAGE
+#define H3QK_SMALL_SAGE 82
+#endif
+template <int MODE>
+constexpr int small_code()
+{
+    return MODE == kOut16 ? H3QK_SMALL_OUT16
+                          : (MODE == kAmax ? H3QK_SMALL_AMAX : (MODE == kCast ? H3QK_SMALL_CAST : H3QK_SMALL_SAGE));
+}
+template <int MODE, int LPR>
+struct Shape {
+    static constexpr bool kSmall = LPR <= 4;
+    static constexpr int W = kSmall ? small_code<MODE>() / 10 : kWarpsPerBlock;  // warps per block
+    static constexpr int MB = kSmall ? small_code<MODE>() % 10 : Tune<MODE>::MB;  // blocks per SM
+    static constexpr int NT = 32 * W;                                          // threads per block
+    static_assert(W >= 1 && W <= 32 && MB >= 1, "block shape code: warps 1..32, blocks per SM >= 1");
+};
+
+// Dynamic shared memory of one block of an instance: S stages x U head rows x
+// CH chunks x 32 lanes x 16 bytes per warp.
+template <int LPR, int CH, int MODE>
 constexpr size_t stage_bytes()
 {
-    return static_cast<size_t>(kWarpsPerBlock) * Tune<MODE>::S * Tune<MODE>::U * CH * 32 * 16;
+    return static_cast<size_t>(Shape<MODE, LPR>::W) * Tune<MODE>::S * Tune<MODE>::U * CH * 32 * 16;
 }
 
 // Everything a launch needs, passed as one __grid_constant__ parameter.
@@ -571,7 +606,8 @@ __device__ __forceinline__ void emit_e4m3(const uint32_t (&y)[4], float f, uint8
 // writes binary32 Q, binary32 K * kv_scale and binary16 V * kv_scale.
 // ---------------------------------------------------------------------------
 template <bool BF16, int LPR, int CH, int MODE, bool SLICED>
-__global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const __grid_constant__ Params p)
+__global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
+    qkprep_kernel(const __grid_constant__ Params p)
 {
     static_assert(CH == 1 || CH == 2 || CH == 4, "1, 2 or 4 chunks per lane");
     constexpr int TPW = 32 / LPR;
@@ -594,8 +630,9 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
     const int hs_shift = SLICED ? p.hs_shift : 0;
     const int64_t n_items = n_groups << hs_shift;
     const int hs_mask = (1 << hs_shift) - 1;
-    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-    const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+    constexpr int NT = Shape<MODE, LPR>::NT;  // threads per block
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * NT + threadIdx.x) >> 5;
+    const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * NT) >> 5;
 
     // Cast factors (each thread derives them; block 0 publishes the descales).
     float fac[3] = {1.0f, 1.0f, 1.0f};
@@ -625,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
     // ws[part][c][q*8 + k] = weight of channel 8*(c + q*LPR) + k (zero past
     // the head), so a lane reads its CH*8 weights as 2*CH float4.
     __shared__ __align__(16) float ws[2][LPR][CH * 8];
-    for (int t = threadIdx.x; t < 2 * LPR * CH * 8; t += kThreads) {
+    for (int t = threadIdx.x; t < 2 * LPR * CH * 8; t += NT) {
         const int part = t / (LPR * CH * 8), cc = (t / (CH * 8)) % LPR, q = (t / 8) % CH, k = t % 8;
         const float* w = part == 0 ? p.wq : p.wk;
         const int chunk = cc + q * LPR;
@@ -971,7 +1008,7 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
     if constexpr (S > 0) cp_async_wait<0>();  // only empty groups remain; keep the exit clean
 
     if constexpr (MODE == kAmax) {
-        __shared__ float red[3][kWarpsPerBlock];
+        __shared__ float red[3][Shape<MODE, LPR>::W];
 #pragma unroll
         for (int t = 0; t < 3; ++t) {
             float m = hmax2_to_float<BF16>(am[t]);
@@ -983,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::MB) qkprep_kernel(const 
         if (threadIdx.x < 3 && p.slot[threadIdx.x] >= 0) {
             float m = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kWarpsPerBlock; ++w) m = fmaxf(m, red[threadIdx.x][w]);
+            for (int w = 0; w < Shape<MODE, LPR>::W; ++w) m = fmaxf(m, red[threadIdx.x][w]);
             // Non-negative binary32 values order like their bit patterns.
             if (m > 0.0f) atomicMax(p.amax_words + p.slot[threadIdx.x], __float_as_uint(m));
         }

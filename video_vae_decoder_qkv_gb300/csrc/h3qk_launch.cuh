@@ -55,7 +55,9 @@ constexpr int waves()
 template <bool BF16, int LPR, int CH, int MODE, bool SLICED>
 cudaError_t launch_sliced(const h3qk::Params& p, cudaStream_t st)
 {
-    constexpr size_t smem = h3qk::stage_bytes<CH, MODE>();
+    constexpr size_t smem = h3qk::stage_bytes<LPR, CH, MODE>();
+    constexpr int W = h3qk::Shape<MODE, LPR>::W;
+    constexpr int NT = h3qk::Shape<MODE, LPR>::NT;
     auto* kernel = h3qk::qkprep_kernel<BF16, LPR, CH, MODE, SLICED>;
     if constexpr (smem > 0) {
         static std::mutex mu;
@@ -72,7 +74,7 @@ cudaError_t launch_sliced(const h3qk::Params& p, cudaStream_t st)
     }
     constexpr int64_t tpw = 32 / LPR;
     const int64_t groups = ((p.rows + tpw - 1) / tpw) << (SLICED ? p.hs_shift : 0);
-    const int64_t want = (groups + h3qk::kWarpsPerBlock - 1) / h3qk::kWarpsPerBlock;
+    const int64_t want = (groups + W - 1) / W;
     int64_t cap = static_cast<int64_t>(h3qk_internal_sm_count()) * H3QK_BLOCKS_PER_SM;
     if constexpr (waves<MODE>() > 0) {
         // A whole number of waves of the blocks that fit on an SM at once.
@@ -81,14 +83,14 @@ cudaError_t launch_sliced(const h3qk::Params& p, cudaStream_t st)
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
         if (occ[dev] == 0) {
             int n = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, h3qk::kThreads, smem) != cudaSuccess || n < 1)
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, NT, smem) != cudaSuccess || n < 1)
                 n = 1;
             occ[dev] = n;
         }
         cap = static_cast<int64_t>(h3qk_internal_sm_count()) * occ[dev] * waves<MODE>();
     }
     const int blocks = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
-    kernel<<<blocks, h3qk::kThreads, smem, st>>>(p);
+    kernel<<<blocks, NT, smem, st>>>(p);
     h3qk_internal_count_launch();
     return cudaGetLastError();
 }
