@@ -92,20 +92,34 @@ def test_per_item_valid_lengths(mode):
         assert np.array_equal(sc.cpu().numpy(), want[3])
 
 
+CANARY8 = 0xA5     # e4m3 output fill: padded rows must keep it
+SAT_GEOMETRIES = {
+    "d64_bf16": W.BATCHED_FP8.with_(name="sat", batch=2, seq=306, grid=(1, 18, 17), valid_len=300),
+    "d128_fp16": W.LATENT_65K.with_(name="sat128", batch=2, seq=131, grid=(1, 1, 131), valid_len=127,
+                                    in_dtype=W.FP16),
+}
+
+
+@pytest.mark.parametrize("geometry", list(SAT_GEOMETRIES))
 @pytest.mark.parametrize("scales", [None, (0.01, 0.02, 0.05), (1e-30, 1.0, 1e30)])
-def test_saturation_counts(scales):
+def test_saturation_counts(scales, geometry):
+    """A cast with sat_counts runs its own kernel instance: its counts, and
+    its codes and scales, must equal the oracle's."""
     import torch
 
     mode = "dynamic" if scales is None else "static"
-    spec = W.BATCHED_FP8.with_(name="sat", batch=2, seq=306, grid=(1, 18, 17), valid_len=300,
-                               **MODES[mode])
+    spec = SAT_GEOMETRIES[geometry].with_(**MODES[mode])
     inp = G.inputs(spec)
     qkv, wq, wk, pos = G.to_device(inp)
     counts = torch.zeros(3, dtype=torch.int32, device="cuda")
     st = torch.tensor(scales, dtype=torch.float32, device="cuda") if scales else None
-    _, _, _, sc = prepare(qkv, wq, wk, pos, heads=spec.heads, head_dim=spec.head_dim,
+    shape = (spec.batch, spec.heads, spec.seq, spec.head_dim)
+    out = tuple(torch.full(shape, CANARY8, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+                for _ in range(3))
+    q, k, v, sc = prepare(qkv, wq, wk, pos, heads=spec.heads, head_dim=spec.head_dim,
                           rotary_dim=spec.rotary_dim, batch=spec.batch, valid_len=spec.valid_len,
-                          scale_mode=mode, axis_dims=spec.axis_dims, static_scales=st, sat_counts=counts)
+                          scale_mode=mode, axis_dims=spec.axis_dims, static_scales=st, sat_counts=counts,
+                          out=out)
     torch.cuda.synchronize()
     kw = {"static_scales": tuple(float(x) for x in scales)} if scales else {}
     pb = G.problem(spec, **kw)
@@ -114,6 +128,11 @@ def test_saturation_counts(scales):
     _, inv = oracle.scales(pb, am)
     want = oracle.sat_counts(pb, inp.qkv, inp.wq, inp.wk, inp.pos, inv)
     assert counts.cpu().numpy().astype(np.uint32).tolist() == want.tolist()
+    full = oracle.prepare(pb, inp.qkv, inp.wq, inp.wk, inp.pos,
+                          out=tuple(np.full(shape, CANARY8, np.uint8) for _ in range(3)), threads=G.THREADS)
+    for name, g, w in zip("qkv", (q, k, v), full[:3]):
+        G.assert_codes_equal(G.host_codes(g), w, f"counted cast {geometry} {mode} {name}", nan_kind="e4m3")
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), full[3].view(np.uint32))
 
 
 @pytest.mark.parametrize("kind", ["q", "k", "v"])

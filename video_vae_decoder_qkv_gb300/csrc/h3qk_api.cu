@@ -120,6 +120,8 @@ bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.
 
 cudaError_t launch(bool bf16, int P, int mode, const h3qk::Params& p, cudaStream_t st)
 {
+    // A cast that counts clipped values runs its own instance.
+    if (mode == h3qk::kCast && p.sat_counts) mode = h3qk::kCastCount;
     return bf16 ? h3qk_internal_launch_bf16(P, mode, p, st) : h3qk_internal_launch_fp16(P, mode, p, st);
 }
 

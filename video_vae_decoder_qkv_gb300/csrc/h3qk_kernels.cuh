@@ -68,7 +68,9 @@ constexpr int kWarpsPerBlock = 8;    // head_dim > 64; see Shape for head_dim <=
 #define H3QK_TUNE_SAGE 44204
 #endif
 
-enum Mode : int { kOut16 = 0, kAmax = 1, kCast = 2, kSage = 3 };
+// kCastCount is the cast that also counts clipped values (opts.sat_counts):
+// a separate instance, so that the plain cast carries no counter state.
+enum Mode : int { kOut16 = 0, kAmax = 1, kCast = 2, kSage = 3, kCastCount = 4 };
 
 template <int CODE, int CH_>
 struct TuneT {
@@ -85,6 +87,7 @@ template <> struct Tune<kOut16> : TuneT<H3QK_TUNE_OUT16, H3QK_CH_OUT16> {};
 template <> struct Tune<kAmax> : TuneT<H3QK_TUNE_AMAX, H3QK_CH_AMAX> {};
 template <> struct Tune<kCast> : TuneT<H3QK_TUNE_CAST, H3QK_CH_CAST> {};
 template <> struct Tune<kSage> : TuneT<H3QK_TUNE_SAGE, H3QK_CH_SAGE> {};
+template <> struct Tune<kCastCount> : TuneT<H3QK_TUNE_CAST, H3QK_CH_CAST> {};
 
 // Block shape of the instances whose warps hold 8 or more token rows (LPR <= 4,
 // head_dim <= 64), per mode as a code "W MB": warps per block (1 or 2 digits)
@@ -111,7 +114,8 @@ template <int MODE>
 constexpr int small_code()
 {
     return MODE == kOut16 ? H3QK_SMALL_OUT16
-                          : (MODE == kAmax ? H3QK_SMALL_AMAX : (MODE == kCast ? H3QK_SMALL_CAST : H3QK_SMALL_SAGE));
+                          : (MODE == kAmax ? H3QK_SMALL_AMAX
+                                           : (MODE == kCast || MODE == kCastCount ? H3QK_SMALL_CAST : H3QK_SMALL_SAGE));
 }
 template <int MODE, int LPR>
 struct Shape {
@@ -160,7 +164,7 @@ struct Params {
     int32_t has_v;               // part 2 (V) is copied / cast
     int32_t slot[3];             // amax / scale / count slot of each part, -1 if unused
     const int32_t* valid_lens;   // per-item valid lengths (device), or null
-    unsigned int* sat_counts;    // cast mode: clipped-element counters (device), or null
+    unsigned int* sat_counts;    // kCastCount: clipped-element counters (device); null otherwise
     float kv_scale;              // sage mode: factor of K (binary32 out) and V (binary16 out)
     int64_t pf_span;             // elements of an input row the call reads ([0, pf_span))
     int32_t hs_shift;            // sliced launches: log2 of the head slices per row group
@@ -602,8 +606,9 @@ __device__ __forceinline__ void emit_e4m3(const uint32_t (&y)[4], float f, uint8
 // [B, H, S, D] or token-major [B, S, H, D]).  The reduction tree is the same for every (LPR, CH): the first
 // halving level (chunk c + chunk c+LPR) is in-lane, the rest are xor shuffles.
 // MODE kOut16 writes 16-bit head-major outputs; kAmax reduces max |y| per
-// tensor; kCast writes e4m3 codes under the dynamic or static factors; kSage
-// writes binary32 Q, binary32 K * kv_scale and binary16 V * kv_scale.
+// tensor; kCast writes e4m3 codes under the dynamic or static factors, and
+// kCastCount does the same and adds the clipped-value counts; kSage writes
+// binary32 Q, binary32 K * kv_scale and binary16 V * kv_scale.
 // ---------------------------------------------------------------------------
 template <bool BF16, int LPR, int CH, int MODE, bool SLICED>
 __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
@@ -623,7 +628,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     for (int q = 0; q < CH; ++q) on[q] = c + q * LPR < p.chunks;
     const int H = p.heads;
     const int D = p.head_dim;
-    const bool count_sat = MODE == kCast && p.sat_counts != nullptr;
+    constexpr bool kCastMode = MODE == kCast || MODE == kCastCount;
+    constexpr bool count_sat = MODE == kCastCount;
     const int64_t n_groups = (p.rows + TPW - 1) / TPW;
     // Work items: a row group, or (SLICED, for calls too small to fill the
     // GPU) one of 2^hs_shift slices of hs_heads heads of a row group.
@@ -636,7 +642,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
 
     // Cast factors (each thread derives them; block 0 publishes the descales).
     float fac[3] = {1.0f, 1.0f, 1.0f};
-    if constexpr (MODE == kCast) {
+    if constexpr (kCastMode) {
 #pragma unroll
         for (int t = 0; t < 3; ++t) {
             if (p.slot[t] < 0) continue;
@@ -932,10 +938,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                             for (int i = 0; i < 4; ++i) am[part] = hmax2_abs<BF16>(am[part], y[q][i]);
                         } else {
                             uint8_t* dst = static_cast<uint8_t*>(p.out[part]) + off;
-                            if (count_sat)  // warp-uniform
-                                emit_e4m3<BF16, true>(y[q], fac[part], dst, sat[part]);
-                            else
-                                emit_e4m3<BF16, false>(y[q], fac[part], dst, sat[part]);
+                            emit_e4m3<BF16, count_sat>(y[q], fac[part], dst, sat[part]);
                         }
                     }
                     if constexpr (MODE == kAmax) {
@@ -994,10 +997,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                         } else {
                             const uint32_t yv[4] = {raw[u][q].x, raw[u][q].y, raw[u][q].z, raw[u][q].w};
                             uint8_t* dst = static_cast<uint8_t*>(p.out[2]) + off;
-                            if (count_sat)  // warp-uniform
-                                emit_e4m3<BF16, true>(yv, fac[2], dst, sat[2]);
-                            else
-                                emit_e4m3<BF16, false>(yv, fac[2], dst, sat[2]);
+                            emit_e4m3<BF16, count_sat>(yv, fac[2], dst, sat[2]);
                         }
                     }
                 }
@@ -1025,15 +1025,13 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
             if (m > 0.0f) atomicMax(p.amax_words + p.slot[threadIdx.x], __float_as_uint(m));
         }
     }
-    if constexpr (MODE == kCast) {
-        if (count_sat) {
+    if constexpr (count_sat) {
 #pragma unroll
-            for (int t = 0; t < 3; ++t) {
-                unsigned int n = sat[t];
+        for (int t = 0; t < 3; ++t) {
+            unsigned int n = sat[t];
 #pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-                if (lane == 0 && n > 0 && p.slot[t] >= 0) atomicAdd(p.sat_counts + p.slot[t], n);
-            }
+            for (int o = 16; o >= 1; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+            if (lane == 0 && n > 0 && p.slot[t] >= 0) atomicAdd(p.sat_counts + p.slot[t], n);
         }
     }
 }

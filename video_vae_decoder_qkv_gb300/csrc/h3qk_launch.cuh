@@ -43,7 +43,9 @@ constexpr int waves()
 {
     return MODE == h3qk::kOut16 ? H3QK_WAVES_OUT16
                                 : (MODE == h3qk::kAmax ? H3QK_WAVES_AMAX
-                                                       : (MODE == h3qk::kCast ? H3QK_WAVES_CAST : H3QK_WAVES_SAGE));
+                                                       : (MODE == h3qk::kCast || MODE == h3qk::kCastCount
+                                                              ? H3QK_WAVES_CAST
+                                                              : H3QK_WAVES_SAGE));
 }
 
 // One launch of a mode.  The grid covers the call's row groups (32/LPR
@@ -148,6 +150,7 @@ cudaError_t launch_m(int P, int mode, const h3qk::Params& p, cudaStream_t st)
     case h3qk::kOut16: return launch_p<BF16, h3qk::kOut16>(P, p, st);
     case h3qk::kAmax: return launch_p<BF16, h3qk::kAmax>(P, p, st);
     case h3qk::kSage: return launch_p<BF16, h3qk::kSage>(P, p, st);
+    case h3qk::kCastCount: return launch_p<BF16, h3qk::kCastCount>(P, p, st);
     default: return launch_p<BF16, h3qk::kCast>(P, p, st);
     }
 }
