@@ -96,7 +96,8 @@ template <> struct Tune<kCastCount> : TuneT<H3QK_TUNE_CAST, H3QK_CH_CAST> {};
 // twice as much per byte as at head_dim 128.  Measured best: 16-bit output
 // in blocks of 10 warps, 2 per SM (20 warps of up to 96 registers, against
 // 8 x 2); amax and cast in blocks of 5 warps, 4 per SM (20 warps of up to 96
-// registers, against 24 warps of 80 that spill).  The larger heads keep
+// registers, against 24 warps of 80 that spill); the sage outputs in blocks
+// of 4 warps, 4 per SM (16 warps in smaller blocks).  The larger heads keep
 // 8 warps per block and the MIN_BLOCKS digit of their tuning code.
 #ifndef H3QK_SMALL_OUT16
 #define H3QK_SMALL_OUT16 102
@@ -108,7 +109,7 @@ template <> struct Tune<kCastCount> : TuneT<H3QK_TUNE_CAST, H3QK_CH_CAST> {};
 #define H3QK_SMALL_CAST 54
 #endif
 #ifndef H3QK_SMALL_SAGE
-#define H3QK_SMALL_SAGE 82
+#define H3QK_SMALL_SAGE 44
 #endif
 template <int MODE>
 constexpr int small_code()
