@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 namespace h3qk {
 
@@ -89,6 +90,34 @@ template <> struct Tune<kCast> : TuneT<H3QK_TUNE_CAST, H3QK_CH_CAST> {};
 template <> struct Tune<kSage> : TuneT<H3QK_TUNE_SAGE, H3QK_CH_SAGE> {};
 template <> struct Tune<kCastCount> : TuneT<H3QK_TUNE_CAST, H3QK_CH_CAST> {};
 
+// Tuning codes of the instances whose warps hold 8 or more token rows (LPR <=
+// 4, head_dim <= 64), same digits; their MIN_BLOCKS digit is unused (Shape
+// below sets it).  The 16-bit pass takes batches of 2 rows and 3 stages
+// there (4 % faster than 4 rows and 2 stages at this block shape).
+#ifndef H3QK_SMALL_TUNE_OUT16
+#define H3QK_SMALL_TUNE_OUT16 24203
+#endif
+#ifndef H3QK_SMALL_TUNE_AMAX
+#define H3QK_SMALL_TUNE_AMAX H3QK_TUNE_AMAX
+#endif
+#ifndef H3QK_SMALL_TUNE_CAST
+#define H3QK_SMALL_TUNE_CAST H3QK_TUNE_CAST
+#endif
+#ifndef H3QK_SMALL_TUNE_SAGE
+#define H3QK_SMALL_TUNE_SAGE H3QK_TUNE_SAGE
+#endif
+template <int MODE>
+constexpr int small_tune_code()
+{
+    return MODE == kOut16 ? H3QK_SMALL_TUNE_OUT16
+                          : (MODE == kAmax ? H3QK_SMALL_TUNE_AMAX
+                                           : (MODE == kCast || MODE == kCastCount ? H3QK_SMALL_TUNE_CAST
+                                                                                  : H3QK_SMALL_TUNE_SAGE));
+}
+// The tuning an instance uses: its mode's, or the small-head code above.
+template <int MODE, int LPR>
+using TuneL = typename std::conditional<(LPR <= 4), TuneT<small_tune_code<MODE>(), Tune<MODE>::CH>, Tune<MODE>>::type;
+
 // Block shape of the instances whose warps hold 8 or more token rows (LPR <= 4,
 // head_dim <= 64), per mode as a code "W MB": warps per block (1 or 2 digits)
 // and the resident blocks per SM asked of the register allocator.  Their
@@ -97,7 +126,8 @@ template <> struct Tune<kCastCount> : TuneT<H3QK_TUNE_CAST, H3QK_CH_CAST> {};
 // in blocks of 10 warps, 2 per SM (20 warps of up to 96 registers, against
 // 8 x 2); amax and cast in blocks of 5 warps, 4 per SM (20 warps of up to 96
 // registers, against 24 warps of 80 that spill); the sage outputs in blocks
-// of 4 warps, 4 per SM (16 warps in smaller blocks).  The larger heads keep
+// of 4 warps with registers for 4 per SM (its four-stage pipeline takes
+// 64 KB per block, so 3 reside: 12 warps).  The larger heads keep
 // 8 warps per block and the MIN_BLOCKS digit of their tuning code.
 #ifndef H3QK_SMALL_OUT16
 #define H3QK_SMALL_OUT16 102
@@ -132,7 +162,7 @@ struct Shape {
 template <int LPR, int CH, int MODE>
 constexpr size_t stage_bytes()
 {
-    return static_cast<size_t>(Shape<MODE, LPR>::W) * Tune<MODE>::S * Tune<MODE>::U * CH * 32 * 16;
+    return static_cast<size_t>(Shape<MODE, LPR>::W) * TuneL<MODE, LPR>::S * TuneL<MODE, LPR>::U * CH * 32 * 16;
 }
 
 // Everything a launch needs, passed as one __grid_constant__ parameter.
@@ -617,10 +647,10 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
 {
     static_assert(CH == 1 || CH == 2 || CH == 4, "1, 2 or 4 chunks per lane");
     constexpr int TPW = 32 / LPR;
-    constexpr int U = Tune<MODE>::U;    // Q/K head rows per batch of loads
-    constexpr int S = Tune<MODE>::S;    // shared-memory pipeline stages (0 = none)
-    constexpr int UV = S > 0 ? U : Tune<MODE>::UV;  // V head rows per batch (copy only)
-    constexpr int PF = Tune<MODE>::PF;  // L2 prefetch distance in batches
+    constexpr int U = TuneL<MODE, LPR>::U;    // Q/K head rows per batch of loads
+    constexpr int S = TuneL<MODE, LPR>::S;    // shared-memory pipeline stages (0 = none)
+    constexpr int UV = S > 0 ? U : TuneL<MODE, LPR>::UV;  // V head rows per batch (copy only)
+    constexpr int PF = TuneL<MODE, LPR>::PF;  // L2 prefetch distance in batches
     const int lane = threadIdx.x & 31;
     const int sub = lane / LPR;
     const int c = lane % LPR;
