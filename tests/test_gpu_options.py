@@ -97,6 +97,9 @@ SAT_GEOMETRIES = {
     "d64_bf16": W.BATCHED_FP8.with_(name="sat", batch=2, seq=306, grid=(1, 18, 17), valid_len=300),
     "d128_fp16": W.LATENT_65K.with_(name="sat128", batch=2, seq=131, grid=(1, 1, 131), valid_len=127,
                                     in_dtype=W.FP16),
+    # 2,560 row groups of 4 tokens: above the small-call threshold, so the
+    # unsliced counting instance runs
+    "d128_bf16_plain": W.LATENT_65K.with_(name="sat128p", seq=10240, grid=(5, 32, 64), valid_len=10200),
 }
 
 
