@@ -49,8 +49,9 @@ constexpr int waves()
 }
 
 // One launch of a mode.  The grid covers the call's row groups (32/LPR
-// token rows per warp, 8 warps per block), capped at 8 blocks per SM; the
-// kernel grid-strides over the rest.  Modes with a shared-memory pipeline
+// token rows per warp, Shape<MODE, LPR>::W warps per block), capped at 8
+// blocks per SM or at whole waves (waves() above); the kernel grid-strides
+// over the rest.  Modes with a shared-memory pipeline
 // take dynamic shared memory; the kernel's dynamic limit is raised to that
 // size once per device (static and dynamic together may exceed the 48 KB
 // default).
@@ -58,6 +59,7 @@ template <bool BF16, int LPR, int CH, int MODE, bool SLICED>
 cudaError_t launch_sliced(const h3qk::Params& p, cudaStream_t st)
 {
     constexpr size_t smem = h3qk::stage_bytes<LPR, CH, MODE>();
+    static_assert(smem <= 227 * 1024, "a block's pipeline stages exceed the 227 KB of shared memory per block");
     constexpr int W = h3qk::Shape<MODE, LPR>::W;
     constexpr int NT = h3qk::Shape<MODE, LPR>::NT;
     auto* kernel = h3qk::qkprep_kernel<BF16, LPR, CH, MODE, SLICED>;
