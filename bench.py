@@ -549,10 +549,10 @@ def run_ours(args):
     e2e_s = es.elapsed_time(ee) / 1e3
     e2e_max, e2e_bytes = reduce_max_sum(dist, e2e_s, step_bytes * E, dev)
 
+    large = large_configs(dev, measured_peak()[0]) if not args.tokens else None
     variants = variant_ops(dev, stream, qkv, wq, wk, pos, common, spec16)
     extra = adjacent_ops(dev, stream) if not args.tokens else None
     small = small_calls(dev) if not args.tokens else None
-    large = large_configs(dev, measured_peak()[0]) if not args.tokens else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.tokens:
