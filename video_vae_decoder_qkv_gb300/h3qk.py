@@ -140,6 +140,48 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _need(t, name, *, device=None, esz=None, dtypes=None, numel=None, min_numel=None, optional=False):
+    """Reject a caller tensor that does not fit what the library will read or
+    write through its pointer: the C-ABI sees only addresses, so a short or
+    strided buffer would be overrun on the device."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name} must be {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
+    if esz is not None and t.element_size() != esz:
+        raise TypeError(f"{name} must have {esz}-byte elements, got {t.dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{name} must have at least {min_numel} elements, got {t.numel()}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+def _need_rows(x, name, width):
+    """A packed input [tokens, row_stride] whose rows hold `width` values."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D [tokens, row_stride] with unit inner stride")
+    if x.shape[1] < width:
+        raise ValueError(f"{name} rows hold {x.shape[1]} values, the call reads {width}")
+
+
+def _need_common(qkv, norm_wq, norm_wk, positions, *, tokens, heads, head_dim, rotary_dim, n_axes, batch,
+                 valid_lens, device, width_parts=3, weights=("norm_wq", "norm_wk")):
+    import torch
+
+    _need_rows(qkv, "qkv", width_parts * heads * head_dim)
+    for w, name in zip((norm_wq, norm_wk), weights):
+        _need(w, name, device=device, dtypes=(torch.float32,), numel=head_dim)
+    if positions is not None or rotary_dim > 0:
+        _need(positions, "positions", device=device, dtypes=(torch.int32,), numel=tokens * n_axes)
+    _need(valid_lens, "valid_lens", device=device, dtypes=(torch.int32,), numel=batch, optional=True)
+
+
 def prepare(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rotary_dim: int,
             batch: int = 1, valid_len: int | None = None, scale_mode: str = "none",
             n_axes: int | None = None, axis_dims=None, theta: float = 10000.0, eps: float = 1e-6,
@@ -180,12 +222,22 @@ def prepare(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rota
     dev = qkv.device
     layout = {"head_major": HEAD_MAJOR, "token_major": TOKEN_MAJOR}[out_layout]
     shape = (batch, heads, seq, head_dim) if layout == HEAD_MAJOR else (batch, seq, heads, head_dim)
+    _need_common(qkv, norm_wq, norm_wk, positions, tokens=tokens, heads=heads, head_dim=head_dim,
+                 rotary_dim=rotary_dim, n_axes=n_axes, batch=batch, valid_lens=valid_lens, device=dev)
     if out is None:
         tdt = qkv.dtype if out_dt != E4M3 else torch.float8_e4m3fn
         out = tuple(torch.empty(shape, dtype=tdt, device=dev) for _ in range(3))
     q, k, v = out
+    for t, name in zip((q, k, v), ("out[0]", "out[1]", "out[2]")):
+        _need(t, name, device=dev, esz=1 if out_dt == E4M3 else 2, numel=tokens * heads * head_dim)
     if out_dt == E4M3 and out_scales is None:
         out_scales = torch.empty(3, dtype=torch.float32, device=dev)
+    if out_dt == E4M3:
+        _need(out_scales, "out_scales", device=dev, dtypes=(torch.float32,), min_numel=3)
+    if mode == SCALE_STATIC:
+        _need(static_scales, "static_scales", device=dev, dtypes=(torch.float32,), min_numel=3)
+    _need(sat_counts, "sat_counts", device=dev, esz=4, min_numel=3, optional=True)
+    _need(workspace, "workspace", device=dev, optional=True)
     if mode == SCALE_DYNAMIC and workspace is None:
         workspace = torch.empty(int(lib().h3qk_workspace_bytes()) // 4, dtype=torch.int32, device=dev)
     o = default_opts()
@@ -259,12 +311,16 @@ def prepare_sage(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int,
         n_axes = positions.shape[1] if positions is not None and positions.dim() == 2 else 3
     layout = {"head_major": HEAD_MAJOR, "token_major": TOKEN_MAJOR}[out_layout]
     shape = (batch, heads, seq, head_dim) if layout == HEAD_MAJOR else (batch, seq, heads, head_dim)
+    dev = qkv.device
+    _need_common(qkv, norm_wq, norm_wk, positions, tokens=tokens, heads=heads, head_dim=head_dim,
+                 rotary_dim=rotary_dim, n_axes=n_axes, batch=batch, valid_lens=valid_lens, device=dev)
     if out is None:
-        dev = qkv.device
         out = (torch.empty(shape, dtype=torch.float32, device=dev),
                torch.empty(shape, dtype=torch.float32, device=dev),
                torch.empty(shape, dtype=torch.float16, device=dev))
     q, k, v = out
+    for t, name, esz in ((q, "out[0]", 4), (k, "out[1]", 4), (v, "out[2]", 2)):
+        _need(t, name, device=dev, esz=esz, numel=tokens * heads * head_dim)
     o = _opts_for(qkv, n_axes=n_axes, axis_dims=axis_dims, theta=theta, eps=eps, batch=batch)
     o.out_layout = layout
     o.valid_lens = _ptr(valid_lens)
@@ -339,12 +395,21 @@ def prepare_host(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int,
         n_axes = positions.shape[1] if positions is not None and positions.dim() == 2 else 3
     layout = {"head_major": HEAD_MAJOR, "token_major": TOKEN_MAJOR}[out_layout]
     shape = (batch, heads, seq, head_dim) if layout == HEAD_MAJOR else (batch, seq, heads, head_dim)
+    host = qkv.device
+    _need_common(qkv, norm_wq, norm_wk, positions, tokens=tokens, heads=heads, head_dim=head_dim,
+                 rotary_dim=rotary_dim, n_axes=n_axes, batch=batch, valid_lens=valid_lens, device=host)
     if out is None:
         tdt = qkv.dtype if out_dt != E4M3 else torch.uint8
         out = tuple(torch.empty(shape, dtype=tdt).pin_memory() for _ in range(3))
     q, k, v = out
+    for t, name in zip((q, k, v), ("out[0]", "out[1]", "out[2]")):
+        _need(t, name, device=host, esz=1 if out_dt == E4M3 else 2, numel=tokens * heads * head_dim)
     if out_dt == E4M3 and out_scales is None:
         out_scales = torch.empty(3, dtype=torch.float32).pin_memory()
+    if out_dt == E4M3:
+        _need(out_scales, "out_scales", device=host, dtypes=(torch.float32,), min_numel=3)
+    if mode == SCALE_STATIC:
+        _need(static_scales, "static_scales", device=host, dtypes=(torch.float32,), min_numel=3)
     o = _opts_for(qkv, n_axes=n_axes, axis_dims=axis_dims, theta=theta, eps=eps, batch=batch)
     o.out_layout = layout
     o.static_scales = _ptr(static_scales)
@@ -399,16 +464,21 @@ def amax(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rotary_
     largest |y| of Q, K and V over the valid rows."""
     import torch
 
-    L = lib()
-    _split_sigs(L)
+    if qkv.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("qkv must be float16 or bfloat16")
     tokens = qkv.shape[0]
     seq = tokens // batch
     if valid_len is None:
         valid_len = seq
     if n_axes is None:
         n_axes = positions.shape[1] if positions is not None and positions.dim() == 2 else 3
+    _need_common(qkv, norm_wq, norm_wk, positions, tokens=tokens, heads=heads, head_dim=head_dim,
+                 rotary_dim=rotary_dim, n_axes=n_axes, batch=batch, valid_lens=None, device=qkv.device)
     if out is None:
         out = torch.empty(3, dtype=torch.float32, device=qkv.device)
+    _need(out, "out", device=qkv.device, dtypes=(torch.float32,), min_numel=3)
+    L = lib()
+    _split_sigs(L)
     o = _opts_for(qkv, n_axes=n_axes, axis_dims=axis_dims, theta=theta, eps=eps, batch=batch)
     if stream is None:
         stream = torch.cuda.current_stream(qkv.device).cuda_stream
@@ -428,20 +498,29 @@ def cast(qkv, norm_wq, norm_wk, positions, amax_t, *, heads: int, head_dim: int,
     ``amax_t`` (float32 [3] CUDA tensor).  Returns (q, k, v, scales)."""
     import torch
 
-    L = lib()
-    _split_sigs(L)
+    if qkv.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("qkv must be float16 or bfloat16")
     tokens = qkv.shape[0]
     seq = tokens // batch
     if valid_len is None:
         valid_len = seq
     if n_axes is None:
         n_axes = positions.shape[1] if positions is not None and positions.dim() == 2 else 3
+    dev = qkv.device
+    _need_common(qkv, norm_wq, norm_wk, positions, tokens=tokens, heads=heads, head_dim=head_dim,
+                 rotary_dim=rotary_dim, n_axes=n_axes, batch=batch, valid_lens=None, device=dev)
+    _need(amax_t, "amax_t", device=dev, dtypes=(torch.float32,), min_numel=3)
     shape = (batch, heads, seq, head_dim)
     if out is None:
-        out = tuple(torch.empty(shape, dtype=torch.float8_e4m3fn, device=qkv.device) for _ in range(3))
+        out = tuple(torch.empty(shape, dtype=torch.float8_e4m3fn, device=dev) for _ in range(3))
     if out_scales is None:
-        out_scales = torch.empty(3, dtype=torch.float32, device=qkv.device)
+        out_scales = torch.empty(3, dtype=torch.float32, device=dev)
     q, k, v = out
+    for t, name in zip((q, k, v), ("out[0]", "out[1]", "out[2]")):
+        _need(t, name, device=dev, esz=1, numel=tokens * heads * head_dim)
+    _need(out_scales, "out_scales", device=dev, dtypes=(torch.float32,), min_numel=3)
+    L = lib()
+    _split_sigs(L)
     o = _opts_for(qkv, n_axes=n_axes, axis_dims=axis_dims, theta=theta, eps=eps, batch=batch)
     if stream is None:
         stream = torch.cuda.current_stream(qkv.device).cuda_stream
@@ -508,11 +587,24 @@ def norm_rope_tensor(x, norm_w, positions, *, kind: str, heads: int, head_dim: i
     out_dt = (FP16 if x.dtype == torch.float16 else BF16) if mode == SCALE_NONE else E4M3
     if n_axes is None:
         n_axes = positions.shape[1] if positions is not None and positions.dim() == 2 else 3
+    dev = x.device
+    _need_rows(x, "x", heads * head_dim)
+    if k != TENSOR_V:
+        _need(norm_w, "norm_w", device=dev, dtypes=(torch.float32,), numel=head_dim)
+        if positions is not None or rotary_dim > 0:
+            _need(positions, "positions", device=dev, dtypes=(torch.int32,), numel=tokens * n_axes)
+    _need(valid_lens, "valid_lens", device=dev, dtypes=(torch.int32,), numel=batch, optional=True)
     if out is None:
         tdt = x.dtype if out_dt != E4M3 else torch.float8_e4m3fn
-        out = torch.empty((batch, seq, heads, head_dim), dtype=tdt, device=x.device)
+        out = torch.empty((batch, seq, heads, head_dim), dtype=tdt, device=dev)
+    _need(out, "out", device=dev, esz=1 if out_dt == E4M3 else 2, numel=tokens * heads * head_dim)
     if out_dt == E4M3 and out_scale is None:
-        out_scale = torch.empty(1, dtype=torch.float32, device=x.device)
+        out_scale = torch.empty(1, dtype=torch.float32, device=dev)
+    if out_dt == E4M3:
+        _need(out_scale, "out_scale", device=dev, dtypes=(torch.float32,), min_numel=1)
+    if mode == SCALE_STATIC:
+        _need(static_scale, "static_scale", device=dev, dtypes=(torch.float32,), min_numel=1)
+    _need(sat_counts, "sat_counts", device=dev, esz=4, min_numel=1, optional=True)
     if mode == SCALE_DYNAMIC and workspace is None:
         workspace = torch.empty(int(L.h3qk_workspace_bytes()) // 4, dtype=torch.int32, device=x.device)
     o = _opts_for(x, n_axes=n_axes, axis_dims=axis_dims, theta=theta, eps=eps, batch=batch)
@@ -552,6 +644,7 @@ def silu_and_mul(x, *, out=None, stream=None):
     f = two_f // 2
     if out is None:
         out = torch.empty((rows, f), dtype=x.dtype, device=x.device)
+    _need(out, "out", device=x.device, esz=2, numel=rows * f)
     if stream is None:
         stream = torch.cuda.current_stream(x.device).cuda_stream
     dt = FP16 if x.dtype == torch.float16 else BF16
@@ -573,9 +666,18 @@ def scaled_residual(residual, branch, scale, *, out=None, stream=None):
         fn.restype = ctypes.c_int
         fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
                        ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    if residual.dim() != 2:
+        raise ValueError("residual must be 2-D [rows, C]")
     rows, C = residual.shape
+    dev = residual.device
+    _need(residual, "residual", device=dev, dtypes=(torch.float32,))
+    _need(branch, "branch", device=dev, dtypes=(torch.float16, torch.bfloat16), numel=rows * C)
+    if scale.numel() not in (1, C):
+        raise ValueError(f"scale must have 1 or {C} elements, got {scale.numel()}")
+    _need(scale, "scale", device=dev, dtypes=(torch.float32,))
     if out is None:
         out = torch.empty_like(residual)
+    _need(out, "out", device=dev, dtypes=(torch.float32,), numel=rows * C)
     if stream is None:
         stream = torch.cuda.current_stream(residual.device).cuda_stream
     dt = FP16 if branch.dtype == torch.float16 else BF16
