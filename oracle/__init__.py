@@ -14,9 +14,11 @@ Every function of the C file cites the page passage it follows; the readings
 taken where the pages are silent are marked "Reading:" there.
 
 Parity status: each step is pinned by closed forms, invariants, brute force
-and hand-worked values in ``tests/test_oracle_*.py``; the composition as a
-whole is "parity unpinned" against the pages, which print no numbers for this
-operation.
+and hand-worked values in ``tests/test_oracle_*.py``, and the whole path by
+the rounding-point error bound of a float64 evaluation of the mathematics.
+The pages print no numbers for this operation, so where they are silent (the
+rounding points, the reduction order, the pair layout) the oracle follows the
+readings marked "Reading:" in the C file.
 """
 from __future__ import annotations
 
