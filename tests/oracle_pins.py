@@ -949,3 +949,124 @@ def pin_sage_kv_scale_and_prefix():
 
 PINS += [pin_sage_vs_float64, pin_sage_v_matches_numpy, pin_sage_agrees_with_16bit_path,
          pin_sage_kv_scale_and_prefix]
+
+
+# --------------------------------------------------------------------------
+# degenerate scales and non-finite values (readings of the cast and of
+# IEEE propagation; the pages are silent on both)
+# --------------------------------------------------------------------------
+
+_FLT_MIN = np.float32(np.finfo(np.float32).tiny)
+_FLT_MAX = np.float32(np.finfo(np.float32).max)
+
+
+def pin_scales_degenerate():
+    """A descale needs a finite, normal, positive binary32.  Zero (either
+    sign), the largest and smallest subnormals, infinities, NaN and negative
+    values give scale = factor = 1 in both modes.  Normal values, the two ends
+    of the normal range included, give amax/448 and 448/amax (dynamic) or the
+    entry and its reciprocal (static).  Each is one IEEE binary32 division,
+    which numpy's float32 arithmetic performs."""
+    bad = [0.0, -0.0, np.nextafter(_FLT_MIN, np.float32(0)), np.float32(1e-40), np.float32(2.0 ** -149),
+           np.inf, -np.inf, np.nan, -1.0, -_FLT_MIN]
+    good = [_FLT_MIN, np.nextafter(_FLT_MIN, np.float32(1)), np.float32(1e-20), np.float32(0.37),
+            np.float32(448.0), np.float32(3.5e37), _FLT_MAX]
+    base = W.TINY.with_(out_kind=W.OUT_E4M3)
+    with np.errstate(over="ignore", divide="ignore", invalid="ignore"):
+        for mode in (oracle.SCALE_DYNAMIC, oracle.SCALE_STATIC):
+            for vals in ([bad[i % len(bad)] for i in range(k, k + 3)] for k in range(len(bad))):
+                a = np.array(vals, np.float32)
+                pb = _problem(base, scale_mode=mode, static_scales=tuple(float(x) for x in a))
+                s, f = oracle.scales(pb, a)
+                assert s.tolist() == [1.0] * 3 and f.tolist() == [1.0] * 3, (mode, vals, s, f)
+            for vals in ([good[i % len(good)] for i in range(k, k + 3)] for k in range(len(good))):
+                a = np.array(vals, np.float32)
+                pb = _problem(base, scale_mode=mode, static_scales=tuple(float(x) for x in a))
+                s, f = oracle.scales(pb, a)
+                if mode == oracle.SCALE_DYNAMIC:
+                    ws, wf = a / np.float32(448.0), np.float32(448.0) / a
+                else:
+                    ws, wf = a, np.float32(1.0) / a
+                assert np.array_equal(s.view(np.uint32), ws.astype(np.float32).view(np.uint32)), (vals, s, ws)
+                assert np.array_equal(f.view(np.uint32), wf.astype(np.float32).view(np.uint32)), (vals, f, wf)
+            # a mixed table: only the degenerate entries fall back
+            a = np.array([0.0, np.float32(0.25), np.nan], np.float32)
+            pb = _problem(base, scale_mode=mode, static_scales=tuple(float(x) for x in a))
+            s, f = oracle.scales(pb, a)
+            mid = (np.float32(0.25) / np.float32(448.0), np.float32(448.0) / np.float32(0.25)) \
+                if mode == oracle.SCALE_DYNAMIC else (np.float32(0.25), np.float32(4.0))
+            assert s.tolist() == [1.0, float(mid[0]), 1.0] and f.tolist() == [1.0, float(mid[1]), 1.0], (s, f)
+
+
+def _bf16_code(x: float) -> int:
+    """bfloat16 code of a value that bfloat16 holds exactly (or inf / NaN)."""
+    return int(np.array([x], np.float32).view(np.uint32)[0] >> 16)
+
+
+def pin_nonfinite_values():
+    """NaN and infinity follow IEEE arithmetic through the path, and the amax
+    leaves NaN out.
+    - A NaN input channel makes the head's sum of squares NaN, so every
+      channel of that Q head comes out NaN, and the other heads are unchanged.
+    - An infinite K channel makes the sum infinite and 1/sqrt of it zero.
+      That channel becomes inf * 0 = NaN, and so does its rotation partner.
+      Every other channel of the head becomes a signed zero.
+    - V passes NaN and infinity through unchanged.
+    - The amax is the maximum |y| over the values that are not NaN: a
+      numpy nanmax over the 16-bit output, never NaN itself.  An infinite V
+      value gives an infinite amax, hence the fallback scale 1 and factor 1.
+      The infinity then saturates to the largest code (0x7E, sign kept), NaN
+      gives a NaN code, and the finite values equal torch's e4m3 conversion.
+    - The single-tensor path's amax skips NaN in the same way."""
+    import torch
+
+    spec = W.TINY.with_(in_dtype=W.BF16, batch=1, seq=12, grid=(1, 3, 4), valid_len=12)
+    inp = W.generate(spec)
+    H, D, HD = spec.heads, spec.head_dim, spec.hd
+    x = inp.qkv.copy()
+    nan16, inf16 = 0x7FC0, _bf16_code(np.inf)
+    x[2, 1 * D + 5] = nan16                 # Q row 2, head 1, channel 5
+    x[4, HD + 0 * D + 7] = inf16            # K row 4, head 0, channel 7 (pair 3, rotated)
+    x[3, 2 * HD + 2 * D + 9] = nan16        # V row 3, head 2, channel 9
+    x[11, 3 * HD - 1] = nan16               # and the very last V value scanned
+    pb16 = _problem(spec, out_kind=0, scale_mode=0)
+    q, k, v, _ = oracle.prepare(pb16, x, inp.wq, inp.wk, inp.pos)
+    q0, k0, v0, _ = oracle.prepare(pb16, inp.qkv, inp.wq, inp.wk, inp.pos)
+    qf, kf, vf = (_widen(t, spec.in_dtype) for t in (q, k, v))
+    assert np.all(np.isnan(qf[0, 1, 2])), "a NaN channel must make its whole Q head NaN"
+    others = [h for h in range(H) if h != 1]
+    assert np.array_equal(q[0, others, 2], q0[0, others, 2]), "other heads of the row must not change"
+    assert np.isnan(kf[0, 0, 4, 7]) and np.isnan(kf[0, 0, 4, 6]), "inf channel and its rotation partner"
+    rest = [d for d in range(D) if d not in (6, 7)]
+    assert np.all(kf[0, 0, 4, rest] == 0.0), "1/sqrt(inf) = 0 zeroes the other channels"
+    assert np.isnan(vf[0, 2, 3, 9]) and v[0, 2, 3, 9] == nan16, "V passes NaN through"
+    nanmax = [float(np.nanmax(np.abs(t))) for t in (qf, kf, vf)]
+    pbd = _problem(spec, out_kind=1, scale_mode=oracle.SCALE_DYNAMIC)
+    am = oracle.amax(pbd, x, inp.wq, inp.wk, inp.pos)
+    assert not np.any(np.isnan(am)), am
+    assert am.astype(np.float64).tolist() == nanmax, (am, nanmax)
+    # an infinite V value: amax inf -> scale = factor = 1 -> inf saturates
+    xi = x.copy()
+    xi[5, 2 * HD + 1 * D + 3] = inf16
+    xi[6, 2 * HD + 3 * D + 0] = _bf16_code(-np.inf)
+    xi[7, 2 * HD + 0 * D + 4] = _bf16_code(300.0)
+    am_i = oracle.amax(pbd, xi, inp.wq, inp.wk, inp.pos)
+    assert am_i[2] == np.inf and am_i[0] == am[0] and am_i[1] == am[1], am_i
+    q8, k8, v8, sc = oracle.prepare(pbd, xi, inp.wq, inp.wk, inp.pos)
+    assert sc[2] == 1.0 and sc[0] == np.float32(am[0]) / np.float32(448.0), sc
+    assert v8[0, 1, 5, 3] == 0x7E and v8[0, 3, 6, 0] == 0xFE, (v8[0, 1, 5, 3], v8[0, 3, 6, 0])
+    assert (v8[0, 2, 3, 9] & 0x7F) == 0x7F, "NaN must give a NaN code"
+    vv = _widen(oracle.prepare(pb16, xi, inp.wq, inp.wk, inp.pos)[2], spec.in_dtype).astype(np.float32)
+    fin = np.isfinite(vv)
+    ref = torch.from_numpy(vv[fin]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(v8[fin], ref)
+    assert np.all((q8[0, 1, 2] & 0x7F) == 0x7F), "the NaN Q head must stay NaN after the cast"
+    # the single-tensor path: its amax skips NaN as well
+    xt = np.ascontiguousarray(x[:, 2 * HD:3 * HD])
+    pbt = oracle.Problem(batch=1, seq=12, heads=H, head_dim=D, rotary_dim=spec.rotary_dim,
+                         in_dtype=spec.in_dtype, tensor=True, out_kind=1, scale_mode=1)
+    _, scale = oracle.tensor_prepare(pbt, 2, xt, None, inp.pos)
+    assert scale == np.float32(np.float32(nanmax[2]) / np.float32(448.0)), (scale, nanmax[2])
+
+
+PINS += [pin_scales_degenerate, pin_nonfinite_values]

@@ -107,6 +107,20 @@ MUTANTS = [
                                    "memset(dst + R, 0, sizeof(float) * (size_t)(D - R));")]),
     ("f16 widening bias", [("else v = ldexpf((float)(man | 0x400), ex - 25);",
                             "else v = ldexpf((float)(man | 0x400), ex - 24);")]),
+    ("scale accepts subnormals", [("return s >= FLT_MIN && s <= FLT_MAX;", "return s > 0.0f && s <= FLT_MAX;")]),
+    ("scale accepts infinity", [("return s >= FLT_MIN && s <= FLT_MAX;", "return s >= FLT_MIN;")]),
+    ("smallest normal scale rejected", [("return s >= FLT_MIN && s <= FLT_MAX;",
+                                         "return s > FLT_MIN && s <= FLT_MAX;")]),
+    ("zero amax gives descale 0", [("i = 448.0f / a;\n            } else {\n                s = 1.0f;",
+                                    "i = 448.0f / a;\n            } else {\n                s = 0.0f;")]),
+    ("degenerate static entry keeps its factor", [("i = 1.0f / tab;\n            } else {\n                s = 1.0f;\n"
+                                                   "                i = 1.0f;",
+                                                   "i = 1.0f / tab;\n            } else {\n                s = 1.0f;\n"
+                                                   "                i = 1.0f / tab;")]),
+    ("amax keeps NaN", [("if (a > m[t]) m[t] = a;", "if (!(a <= m[t])) m[t] = a;")]),
+    ("single-tensor amax keeps NaN", [("if (a > m) m = a;", "if (!(a <= m)) m = a;")]),
+    ("mean square clamped away from zero", [("float t = ms + eps;", "float t = fmaxf(ms + eps, 1e-30f);")]),
+    ("infinite sum clamped", [("float rt = sqrtf(t);", "float rt = sqrtf(fminf(t, FLT_MAX));")]),
 ]
 
 _CHILD = r"""
