@@ -10,9 +10,9 @@
  *
  * Pages that define the operation:
  *  - TensorRT-LLM pull request #21485, "cuDNN FP8 attention path for
- *    MiniMax-H3 on SM107 under Ulysses": Summary bullet 2 (QK-norm, RoPE and
- *    the FP8 per-tensor cast fused into one amax pass and one cast pass;
- *    dynamic scales by default, a static scale table as an option), and the
+ *    MiniMax-H3 on SM107 under Ulysses": Summary, bullet 2 (the operation
+ *    below, whose e4m3 form takes two kernels, a max reduction and then the
+ *    conversion, with the scales computed per call or read from a table), and the
  *    commits that add the fused cast from the packed QKV projection, the
  *    single-tensor norm_rope_tensor variant (identity for V), the per-item
  *    valid length left out of the amax, and the custom-op aliasing fix
@@ -103,7 +103,10 @@ typedef struct h3qk_opts {
     void* workspace;         /* device memory of >= h3qk_workspace_bytes() bytes,
                                 16-byte aligned, required when scale_mode is
                                 DYNAMIC; holds the amax words of one call, so
-                                calls that may overlap need their own */
+                                calls that may overlap need their own.  The
+                                call zeroes it on the stream, so it must not
+                                overlap any input, output, the static table
+                                or sat_counts (H3QK_ERR_ALIAS otherwise) */
     size_t workspace_bytes;  /* size of workspace */
     int32_t out_layout;      /* h3qk_layout of out_q/out_k/out_v: HEAD_MAJOR
                                 [B, H, S, D] (default) or TOKEN_MAJOR [B, S, H, D] */
@@ -114,6 +117,8 @@ typedef struct h3qk_opts {
                                 sat_counts[t] the number of tensor t's values
                                 whose scaled magnitude exceeds 448 (clipped to
                                 the largest code).  The caller zeroes them.
+                                Disjoint from every input, output and the
+                                workspace (H3QK_ERR_ALIAS otherwise).
                                 A counting cast runs its own kernel instance,
                                 a few percent slower than the plain cast; the
                                 codes and scales are the same. */
@@ -164,7 +169,8 @@ size_t h3qk_workspace_bytes(void);
  *   out_q, out_k, out_v  [B, H, S, D] (or [B, S, H, D], opts->out_layout)
  *              contiguous, 2 bytes (16-bit) or 1 byte (e4m3) per element;
  *              16-byte aligned; pairwise disjoint and disjoint from every
- *              input.  Rows past valid_len keep their previous bytes.
+ *              input, from the static table, the workspace and the
+ *              counters.  Rows past valid_len keep their previous bytes.
  *   out_scales float[3] descales (q, k, v) written in e4m3 modes (NULL
  *              allowed with scale_mode NONE); never the static table itself.
  *   opts       NULL or see h3qk_opts.
@@ -209,8 +215,8 @@ h3qk_status h3qk_norm_rope_tensor(const void* x, const float* norm_w, const int3
  * so that a caller whose rows are sharded over several GPUs can all-reduce
  * (MAX) the three amax values between them and cast every shard with the
  * same scales.  This is the exchange the pages make under Ulysses sequence
- * parallelism (TensorRT-LLM PR #21485, commit on the amax all-reduce: "every
- * rank casts and dequantizes with the same scale").  On one GPU,
+ * parallelism (TensorRT-LLM PR #21485, the commit that all-reduces the amax
+ * so that all ranks share one scale per tensor).  On one GPU,
  * h3qk_amax followed by h3qk_cast on the same stream gives the same bytes as
  * h3qk_prepare with H3QK_SCALE_DYNAMIC.
  *
@@ -366,7 +372,7 @@ h3qk_status h3qk_prepare_noalloc(const void* qkv, const float* norm_wq, const fl
  * h3qk_scaled_residual: out[r, c] = residual[r, c] + branch[r, c] * scale[c]
  * (scale_len == channels) or * scale[0] (scale_len == 1); residual, out and
  * scale are FP32, branch 16-bit (branch_dtype); the product is rounded on its
- * own, then the sum ("contraction disabled").  channels is a multiple of 8;
+ * own, then the sum (no multiply-add contraction).  channels is a multiple of 8;
  * residual, branch, out (and a vector scale) 16-byte aligned; out may be
  * residual itself (in place) but must not otherwise overlap an input.
  *
@@ -386,7 +392,7 @@ const char* h3qk_status_string(h3qk_status status);
 int h3qk_last_cuda_error(void);
 
 /* Number of kernel launches the calling thread's h3qk calls have enqueued
- * since the last reset (a "this path ran" counter); reset with
+ * since the last reset (evidence that the CUDA path ran); reset with
  * h3qk_launch_count_reset(). */
 uint64_t h3qk_launch_count(void);
 void h3qk_launch_count_reset(void);

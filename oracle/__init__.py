@@ -515,8 +515,7 @@ def tensor_prepare(pb: Problem, kind: int, x, w, pos, out=None, threads: int = 1
         if pb.scale_mode == SCALE_DYNAMIC:
             am = max([0.0] + list(ex.map(lambda rg: L.h3o_tensor_amax_rows(*args, rg[0], rg[1]), parts)))
         sc, inv = scales(pb, np.array([am, am, am], np.float32))
-        k = 0 if pb.scale_mode == SCALE_STATIC else 0
-        scale, factor = float(sc[k]), float(inv[k])
+        scale, factor = float(sc[0]), float(inv[0])
         list(ex.map(lambda rg: L.h3o_tensor_cast_rows(*args, rg[0], rg[1], factor, _ptr(out)), parts))
     return out, np.float32(scale)
 

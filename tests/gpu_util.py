@@ -148,17 +148,3 @@ def assert_codes_equal(got: np.ndarray, want: np.ndarray, what: str, nan_kind: s
         i = tuple(bad[0])
         raise AssertionError(f"{what}: {len(bad)} codes differ; first at {i}: "
                              f"gpu {int(got[i]):#x} oracle {int(want[i]):#x}")
-
-
-def sample_rows(spec: W.Spec, n_random: int = 48, seed: int = 0) -> np.ndarray:
-    """Rows to check at full size: the first and last rows of every item,
-    the last valid row, rows around warp/block boundaries, random rows."""
-    rng = np.random.default_rng(seed)
-    S, B = spec.seq, spec.batch
-    rows = set()
-    for b in range(B):
-        for s in (0, 1, 2, 3, 15, 16, 31, 32, 127, 128, spec.valid_len - 1, S - 1):
-            if 0 <= s < S:
-                rows.add(b * S + s)
-    rows.update(rng.integers(0, B * S, n_random).tolist())
-    return np.array(sorted(rows), np.int64)

@@ -14,6 +14,7 @@ A = 0x10000000          # fake, 256-byte aligned device addresses
 QKV, WQ, WK, POS = A, A + 0x1000000, A + 0x1001000, A + 0x1002000
 OQ, OK_, OV, SC, TAB, WS = (A + 0x2000000, A + 0x3000000, A + 0x4000000, A + 0x5000000,
                             A + 0x5001000, A + 0x5002000)
+VL = A + 0x5003000
 
 
 @pytest.fixture(scope="module")
@@ -139,6 +140,22 @@ def test_misaligned(kw):
     dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_STATIC, out_scales=TAB, opts=opts(static_scales=TAB)),
     dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC,
          opts=opts(workspace=OQ + 16, workspace_bytes=16)),
+    # the workspace is zeroed on the stream: it may not overlap any input
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC,
+         opts=opts(workspace=QKV + 4096, workspace_bytes=16)),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC,
+         opts=opts(workspace=WQ, workspace_bytes=16)),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC,
+         opts=opts(workspace=POS + 32, workspace_bytes=16)),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC, valid_len=N // 2,
+         opts=opts(workspace=VL, workspace_bytes=16, valid_lens=VL, batch=2)),
+    # the counters are written: not over an input, the table or the workspace
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC,
+         opts=opts(workspace=WS, workspace_bytes=16, sat_counts=WS + 4)),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_STATIC, out_scales=SC,
+         opts=opts(static_scales=TAB, sat_counts=TAB + 4)),
+    dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_STATIC, out_scales=SC,
+         opts=opts(static_scales=TAB, sat_counts=QKV + 64)),
 ])
 def test_aliasing_outputs(kw):
     assert call(**kw) == h3qk.ERR_ALIAS
@@ -295,3 +312,54 @@ def _vae(fn, **kw):
 ])
 def test_vae_ops_check_arguments(fn, kw, want):
     assert _vae(fn, **kw) == want
+
+
+def _tensor_call(**kw):
+    """h3qk_norm_rope_tensor on fake addresses (kind Q, e4m3 dynamic)."""
+    import ctypes as C
+
+    L = h3qk.lib()
+    fn = L.h3qk_norm_rope_tensor
+    P, I32, I64 = C.c_void_p, C.c_int32, C.c_int64
+    fn.restype = C.c_int
+    fn.argtypes = [P, P, P, I64, I32, I32, I32, I64, C.c_int, C.c_int, C.c_int, P, P, C.POINTER(h3qk.Opts), P]
+    o = kw.pop("opts")
+    a = dict(x=QKV, w=WQ, pos=POS, out=OQ, scale=SC)
+    a.update(kw)
+    return fn(a["x"], a["w"], a["pos"], N, H, D, R, N, h3qk.TENSOR_Q, h3qk.E4M3, h3qk.SCALE_DYNAMIC,
+              a["out"], a["scale"], C.byref(o), None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(opts=opts(workspace=QKV + 256, workspace_bytes=16)), h3qk.ERR_ALIAS),
+    (dict(opts=opts(workspace=WQ + 16, workspace_bytes=16)), h3qk.ERR_ALIAS),
+    (dict(opts=opts(workspace=POS, workspace_bytes=16)), h3qk.ERR_ALIAS),
+    (dict(opts=opts(workspace=WS, workspace_bytes=16, sat_counts=WS + 8)), h3qk.ERR_ALIAS),
+    (dict(opts=opts(workspace=WS, workspace_bytes=16, sat_counts=QKV)), h3qk.ERR_ALIAS),
+    (dict(opts=opts(workspace=OQ + 32, workspace_bytes=16)), h3qk.ERR_ALIAS),
+    (dict(opts=opts(workspace=WS, workspace_bytes=16)), h3qk.ERR_CUDA),
+])
+def test_single_tensor_workspace_aliasing(kw, want):
+    assert _tensor_call(**kw) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC,
+          opts=opts(workspace=WS, workspace_bytes=16, sat_counts=WS + 16)), h3qk.ERR_CUDA),
+    (dict(out_dtype=h3qk.E4M3, scale_mode=h3qk.SCALE_DYNAMIC, out_scales=SC,
+          opts=opts(workspace=WS, workspace_bytes=16)), h3qk.ERR_CUDA),
+])
+def test_disjoint_workspace_and_counters_pass_the_checks(kw, want):
+    """Neighbouring but disjoint scratch buffers pass every host check (the
+    call then fails only at the launch, there being no GPU)."""
+    assert call(**kw) == want
+
+
+def test_split_cast_counters_not_over_the_amax():
+    import ctypes as C
+
+    L = h3qk.lib()
+    h3qk._split_sigs(L)
+    o = opts(sat_counts=TAB + 4)
+    st = L.h3qk_cast(QKV, WQ, WK, POS, N, H, D, R, N, TAB, OQ, OK_, OV, SC, C.byref(o), None)
+    assert st == h3qk.ERR_ALIAS

@@ -6,8 +6,9 @@ norm + RoPE).  Every call goes through the C-ABI of libh3qk.so.
 - reduced shapes of the five workloads, element by element, sized to span
   many warps and blocks with a ragged tail;
 - the five workloads at full size, in the launch configuration the benchmark
-  times: the oracle's full amax and descales, and sampled rows element by
-  element;
+  times, element by element;
+- the plain (unsliced) kernel instance of every head_dim class, input type
+  and mode, element by element;
 - edge cases: empty calls, valid_len 0 / 1 / S-1, every head_dim class,
   rotary widths and axis splits, padded row strides, batches with ragged
   items, zero / huge / subnormal / unique-code inputs, non-finite inputs,
@@ -66,35 +67,61 @@ FULL = [W.TINY, W.DECODER_TILE, W.BATCHED_FP8, W.LATENT_65K, W.LATENT_65K_E4M3,
 
 
 @pytest.mark.parametrize("spec", FULL, ids=[s.name for s in FULL])
-def test_full_workloads_sampled(spec):
-    """Full-size run in the benchmark's launch configuration; the oracle
-    computes the amax over every valid row (order-free, exact) and the codes
-    of sampled rows."""
+def test_full_workloads_bit_exact(spec):
+    """Every workload at full size, in the launch configuration the benchmark
+    times: every element of Q, K and V, and the descales, against the oracle
+    run over all host cores (bit-exact, like torch.equal on whole tensors);
+    canaries in the padded rows survive."""
+    import torch
+
     inp = G.inputs(spec)
     fill = CANARY8 if spec.out_kind == W.OUT_E4M3 else CANARY16
     q, k, v, sc = G.gpu_prepare(inp, fill=fill)
+    torch.cuda.synchronize()
+    want = G.oracle_full(inp, fill=fill)
+    _check_full(spec, inp, q, k, v, sc, want, fill=fill)
+    del q, k, v, sc, want
+    torch.cuda.empty_cache()
+
+
+def _unsliced_rows(tpw: int) -> int:
+    """Token rows whose row groups fill at least 16 warps per SM, so the call
+    runs the plain (unsliced) kernel instance the large workloads run, plus a
+    ragged tail."""
     import torch
 
-    rows = G.sample_rows(spec)
-    b, s = rows // spec.seq, rows % spec.seq
-    bi, si = torch.from_numpy(b).cuda(), torch.from_numpy(s).cuda()
-    got = [G.host_codes(G.as_codes(t)[bi, :, si, :]) for t in (q, k, v)]
-    kw = {}
-    if spec.scale_mode == W.SCALE_STATIC:
-        kw["static_scales"] = tuple(float(x) for x in inp.static_scales)
-    pb = G.problem(spec, **kw)
-    valid = s < spec.valid_len
-    if spec.out_kind == W.OUT_16B:
-        want = oracle.row16(pb, inp.qkv, inp.wq, inp.wk, inp.pos, rows)
-    else:
-        am = (oracle.amax(pb, inp.qkv, inp.wq, inp.wk, inp.pos, threads=G.THREADS)
-              if spec.scale_mode == W.SCALE_DYNAMIC else np.zeros(3, np.float32))
-        scale, inv = oracle.scales(pb, am)
-        assert np.array_equal(sc.cpu().numpy().view(np.uint32), scale.view(np.uint32)), (sc, scale)
-        want = oracle.cast_rows(pb, inp.qkv, inp.wq, inp.wk, inp.pos, inv, rows)
-    for name, g, w in zip("qkv", got, want):
-        G.assert_codes_equal(g[valid], w[valid], f"{spec.name} {name} sampled rows")
-        assert np.all(g[~valid] == fill), "padded rows were written"
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 16 * sms * tpw + 3 * tpw + 1
+
+
+@pytest.mark.parametrize("head_dim,rotary_dim", [(16, 12), (32, 24), (64, 48), (128, 96), (256, 192)])
+@pytest.mark.parametrize("dtype", [W.FP16, W.BF16])
+@pytest.mark.parametrize("mode", ["16b", "dynamic", "static", "count"])
+def test_unsliced_instances_bit_exact(head_dim, rotary_dim, dtype, mode):
+    """The plain kernel instance of every head_dim class, input type and mode
+    (the ones the full-size workloads run), element by element: enough rows to
+    take the unsliced launch, a ragged last row group and a padded tail."""
+    lpr = max(1, (1 << (head_dim // 8 - 1).bit_length()) // 2)
+    rows = _unsliced_rows(32 // lpr)
+    kw = {"16b": {}, "dynamic": dict(out_kind=W.OUT_E4M3, scale_mode=W.SCALE_DYNAMIC),
+          "static": dict(out_kind=W.OUT_E4M3, scale_mode=W.SCALE_STATIC),
+          "count": dict(out_kind=W.OUT_E4M3, scale_mode=W.SCALE_DYNAMIC)}[mode]
+    spec = W.Spec(f"unsliced{head_dim}", batch=1, seq=rows, heads=3, head_dim=head_dim, rotary_dim=rotary_dim,
+                  grid=(1, 1, rows), in_dtype=dtype, valid_len=rows - 5, outlier_frac=0.01,
+                  outlier_scale=30.0, seed=head_dim + 7, **kw)
+    if mode != "count":
+        _roundtrip(spec)
+        return
+    import torch
+
+    inp = G.inputs(spec)
+    counts = torch.zeros(3, dtype=torch.int32, device="cuda")
+    q, k, v, sc = G.gpu_prepare(inp, fill=CANARY8, sat_counts=counts)
+    want = G.oracle_full(inp, fill=CANARY8)
+    _check_full(spec, inp, q, k, v, sc, want, fill=CANARY8)
+    _, inv = oracle.scales(G.problem(spec), oracle.amax(G.problem(spec), inp.qkv, inp.wq, inp.wk, inp.pos))
+    wc = oracle.sat_counts(G.problem(spec), inp.qkv, inp.wq, inp.wk, inp.pos, inv)
+    assert counts.cpu().numpy().astype(np.uint32).tolist() == wc.tolist()
 
 
 # --------------------------------------------------------------------------

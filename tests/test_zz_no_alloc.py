@@ -68,3 +68,23 @@ def test_noalloc_matches_prepare_on_two_calls_in_a_row():
         assert np.array_equal(got_sc.cpu().numpy().view(np.uint32), want_sc.cpu().numpy().view(np.uint32))
         results.append(got_sc.cpu().numpy())
     assert results[1][0] < results[0][0], "the second call must have the smaller amax"
+
+
+def test_noalloc_leaves_device_memory_unchanged():
+    """The property the entry point exists for: a dynamic call allocates no
+    device memory.  After a warm-up call of the same shape (which may load the
+    kernels' code on first use), free device memory is the same before and
+    after a call and a synchronize."""
+    import torch
+
+    spec = W.BATCHED_FP8.with_(name="noalloc_mem", batch=2, seq=306, grid=(1, 18, 17), valid_len=300, seed=23)
+    dev = G.to_device(G.inputs(spec))
+    outs, sc = _buffers(spec)
+    _call(h3qk.prepare_noalloc_ptr, spec, dev, outs, sc)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        _call(h3qk.prepare_noalloc_ptr, spec, dev, outs, sc)
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert free1 == free0, (free0, free1)

@@ -250,6 +250,19 @@ bool overlaps_inputs(const Plan& pl, Range r)
     return false;
 }
 
+// The buffers a call writes besides its outputs (the amax workspace, zeroed
+// on the stream before the amax pass, and the saturation counters) must not
+// overlap an input, the static table or each other.  extra = {static table,
+// workspace, counters}, each an empty range when the call does not use it.
+bool scratch_overlaps(const Plan& pl, const Range (&extra)[3])
+{
+    for (int k = 1; k < 3; ++k) {
+        if (overlaps_inputs(pl, extra[k])) return true;
+        if (overlap(extra[k], extra[0])) return true;
+    }
+    return overlap(extra[1], extra[2]);
+}
+
 // Zero the amax words, then run the amax pass (skipped when no row is valid).
 cudaError_t launch_amax_init(unsigned int* words, cudaStream_t st)
 {
@@ -328,7 +341,7 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
         for (int k = 0; k < 3; ++k)
             if (overlap(outs[i], extra[k])) return H3QK_ERR_ALIAS;
     }
-    if (e4m3 && o.sat_counts && overlaps_inputs(pl, extra[2])) return H3QK_ERR_ALIAS;
+    if (scratch_overlaps(pl, extra)) return H3QK_ERR_ALIAS;
 
     h3qk::Params& p = pl.p;
     p.out[0] = out_q;
@@ -421,6 +434,7 @@ h3qk_status h3qk_norm_rope_tensor(const void* x, const float* norm_w, const int3
     if (overlap(ro, rs) || overlaps_inputs(pl, ro) || overlaps_inputs(pl, rs)) return H3QK_ERR_ALIAS;
     for (int k = 0; k < 3; ++k)
         if (overlap(ro, extra[k]) || overlap(rs, extra[k])) return H3QK_ERR_ALIAS;
+    if (scratch_overlaps(pl, extra)) return H3QK_ERR_ALIAS;
 
     h3qk::Params& p = pl.p;
     const int t = static_cast<int>(kind);
@@ -486,7 +500,8 @@ h3qk_status h3qk_cast(const void* qkv, const float* norm_wq, const float* norm_w
     p.scale_words = reinterpret_cast<const unsigned int*>(amax);
     p.dynamic = 1;
     if (o.sat_counts) {
-        if (overlaps_inputs(pl, range_of(o.sat_counts, 12))) return H3QK_ERR_ALIAS;
+        if (overlaps_inputs(pl, range_of(o.sat_counts, 12)) || overlap(range_of(o.sat_counts, 12), amax_r))
+            return H3QK_ERR_ALIAS;
         for (int i = 0; i < 4; ++i)
             if (overlap(outs[i], range_of(o.sat_counts, 12))) return H3QK_ERR_ALIAS;
         p.sat_counts = o.sat_counts;

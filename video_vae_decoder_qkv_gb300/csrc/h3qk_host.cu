@@ -45,14 +45,24 @@ h3qk_status host_streams(HostStreams** out)
     std::lock_guard<std::mutex> lock(g_host_mu);
     HostStreams& h = g_host[dev];
     if (!h.ready) {
+        // A handle made by an earlier, failed attempt is kept and not made
+        // again, so a retry after a failure leaks nothing.
         for (auto& st : h.s)
-            if ((e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking)) != cudaSuccess) return h3qk_internal_fail_cuda(e);
-        cudaEvent_t* evs[] = {&h.start, &h.done, &h.last};
-        for (auto* ev : evs)
-            if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return h3qk_internal_fail_cuda(e);
+            if (!st && (e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking)) != cudaSuccess) {
+                st = nullptr;
+                return h3qk_internal_fail_cuda(e);
+            }
+        auto make_event = [&](cudaEvent_t* ev) {
+            if (*ev) return cudaSuccess;
+            const cudaError_t r = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+            if (r != cudaSuccess) *ev = nullptr;
+            return r;
+        };
+        for (cudaEvent_t* ev : {&h.start, &h.done, &h.last})
+            if ((e = make_event(ev)) != cudaSuccess) return h3qk_internal_fail_cuda(e);
         for (int k = 0; k < kHostSlots; ++k)
             for (cudaEvent_t* ev : {&h.in[k], &h.cmp[k], &h.out[k]})
-                if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return h3qk_internal_fail_cuda(e);
+                if ((e = make_event(ev)) != cudaSuccess) return h3qk_internal_fail_cuda(e);
         h.ready = true;
     }
     *out = &h;

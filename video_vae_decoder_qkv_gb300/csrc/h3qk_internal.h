@@ -55,6 +55,9 @@ H3QK_HIDDEN h3qk_status plan_inputs(const void* qkv, const float* norm_wq, const
                                     int32_t rotary_dim, int64_t valid_len, int default_in, const h3qk_opts& o,
                                     h3qk_stream_t stream, Plan* plan, int parts = 3);
 H3QK_HIDDEN bool overlaps_inputs(const Plan& pl, Range r);
+// True when the workspace or the counters of extra = {static table, workspace,
+// counters} overlap an input, the static table or each other.
+H3QK_HIDDEN bool scratch_overlaps(const Plan& pl, const Range (&extra)[3]);
 // Zero the amax words, then run the amax pass.
 H3QK_HIDDEN h3qk_status run_amax(const Plan& pl);
 // The fused kernel of `mode` on the plan's input type.

@@ -261,9 +261,10 @@ def prepare(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rota
         stream = torch.cuda.current_stream(dev).cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
-    st = prepare_ptr(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens,
-                     heads, head_dim, rotary_dim, valid_len, out_dt, mode, q.data_ptr(),
-                     k.data_ptr(), v.data_ptr(), _ptr(out_scales) if out_dt == E4M3 else None, o, stream)
+    with torch.cuda.device(dev):  # the library keys its caches on the current device
+        st = prepare_ptr(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens,
+                         heads, head_dim, rotary_dim, valid_len, out_dt, mode, q.data_ptr(),
+                         k.data_ptr(), v.data_ptr(), _ptr(out_scales) if out_dt == E4M3 else None, o, stream)
     if st != OK:
         raise H3QKError(st, status_string(st), int(lib().h3qk_last_cuda_error()))
     return q, k, v, (out_scales if out_dt == E4M3 else None)
@@ -328,9 +329,10 @@ def prepare_sage(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int,
         stream = torch.cuda.current_stream(qkv.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
-    st = prepare_sage_ptr(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens,
-                          heads, head_dim, rotary_dim, valid_len, float(kv_scale), q.data_ptr(), k.data_ptr(),
-                          v.data_ptr(), o, stream)
+    with torch.cuda.device(dev):  # the library keys its caches on the current device
+        st = prepare_sage_ptr(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens,
+                              heads, head_dim, rotary_dim, valid_len, float(kv_scale), q.data_ptr(), k.data_ptr(),
+                              v.data_ptr(), o, stream)
     if st != OK:
         raise H3QKError(st, status_string(st), int(lib().h3qk_last_cuda_error()))
     return q, k, v
@@ -422,10 +424,11 @@ def prepare_host(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int,
         stream = torch.cuda.current_stream(dev).cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
-    st = prepare_host_ptr(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens, heads,
-                          head_dim, rotary_dim, valid_len, out_dt, mode, q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                          _ptr(out_scales) if out_dt == E4M3 else None, o, workspace.data_ptr(),
-                          workspace.numel() * workspace.element_size(), stream)
+    with torch.cuda.device(dev):  # the library keys its caches on the current device
+        st = prepare_host_ptr(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens, heads,
+                              head_dim, rotary_dim, valid_len, out_dt, mode, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                              _ptr(out_scales) if out_dt == E4M3 else None, o, workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), stream)
     if st != OK:
         raise H3QKError(st, status_string(st), int(lib().h3qk_last_cuda_error()))
     return q, k, v, (out_scales if out_dt == E4M3 else None)
@@ -484,8 +487,9 @@ def amax(qkv, norm_wq, norm_wk, positions, *, heads: int, head_dim: int, rotary_
         stream = torch.cuda.current_stream(qkv.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
-    st = int(L.h3qk_amax(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens,
-                         heads, head_dim, rotary_dim, valid_len, out.data_ptr(), ctypes.byref(o), stream))
+    with torch.cuda.device(qkv.device):  # the library keys its caches on the current device
+        st = int(L.h3qk_amax(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens,
+                             heads, head_dim, rotary_dim, valid_len, out.data_ptr(), ctypes.byref(o), stream))
     if st != OK:
         raise H3QKError(st, status_string(st), int(L.h3qk_last_cuda_error()))
     return out
@@ -526,9 +530,10 @@ def cast(qkv, norm_wq, norm_wk, positions, amax_t, *, heads: int, head_dim: int,
         stream = torch.cuda.current_stream(qkv.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
-    st = int(L.h3qk_cast(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens,
-                         heads, head_dim, rotary_dim, valid_len, amax_t.data_ptr(), q.data_ptr(),
-                         k.data_ptr(), v.data_ptr(), out_scales.data_ptr(), ctypes.byref(o), stream))
+    with torch.cuda.device(qkv.device):  # the library keys its caches on the current device
+        st = int(L.h3qk_cast(qkv.data_ptr(), norm_wq.data_ptr(), norm_wk.data_ptr(), _ptr(positions), tokens,
+                             heads, head_dim, rotary_dim, valid_len, amax_t.data_ptr(), q.data_ptr(),
+                             k.data_ptr(), v.data_ptr(), out_scales.data_ptr(), ctypes.byref(o), stream))
     if st != OK:
         raise H3QKError(st, status_string(st), int(L.h3qk_last_cuda_error()))
     return q, k, v, out_scales
@@ -618,9 +623,10 @@ def norm_rope_tensor(x, norm_w, positions, *, kind: str, heads: int, head_dim: i
         stream = torch.cuda.current_stream(x.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
-    st = int(fn(x.data_ptr(), _ptr(norm_w), _ptr(positions), tokens, heads, head_dim, rotary_dim, valid_len,
-                k, out_dt, mode, out.data_ptr(), _ptr(out_scale) if out_dt == E4M3 else None,
-                ctypes.byref(o), stream))
+    with torch.cuda.device(x.device):  # the library keys its caches on the current device
+        st = int(fn(x.data_ptr(), _ptr(norm_w), _ptr(positions), tokens, heads, head_dim, rotary_dim, valid_len,
+                    k, out_dt, mode, out.data_ptr(), _ptr(out_scale) if out_dt == E4M3 else None,
+                    ctypes.byref(o), stream))
     if st != OK:
         raise H3QKError(st, status_string(st), int(L.h3qk_last_cuda_error()))
     return out, (out_scale if out_dt == E4M3 else None)
@@ -648,7 +654,8 @@ def silu_and_mul(x, *, out=None, stream=None):
     if stream is None:
         stream = torch.cuda.current_stream(x.device).cuda_stream
     dt = FP16 if x.dtype == torch.float16 else BF16
-    st = int(fn(x.data_ptr(), dt, rows, f, x.stride(0), out.data_ptr(), stream))
+    with torch.cuda.device(x.device):  # the library keys its caches on the current device
+        st = int(fn(x.data_ptr(), dt, rows, f, x.stride(0), out.data_ptr(), stream))
     if st != OK:
         raise H3QKError(st, status_string(st), int(L.h3qk_last_cuda_error()))
     return out
@@ -681,8 +688,9 @@ def scaled_residual(residual, branch, scale, *, out=None, stream=None):
     if stream is None:
         stream = torch.cuda.current_stream(residual.device).cuda_stream
     dt = FP16 if branch.dtype == torch.float16 else BF16
-    st = int(fn(residual.data_ptr(), branch.data_ptr(), dt, scale.data_ptr(), rows, C, scale.numel(),
-                out.data_ptr(), stream))
+    with torch.cuda.device(residual.device):  # the library keys its caches on the current device
+        st = int(fn(residual.data_ptr(), branch.data_ptr(), dt, scale.data_ptr(), rows, C, scale.numel(),
+                    out.data_ptr(), stream))
     if st != OK:
         raise H3QKError(st, status_string(st), int(L.h3qk_last_cuda_error()))
     return out
