@@ -206,6 +206,8 @@ h3qk_status plan_inputs(const void* qkv, const float* norm_wq, const float* norm
     p.chunks = head_dim / 8;
     p.eps = o.eps;
     p.inv_d = (head_dim & (head_dim - 1)) == 0 ? 1.0f / static_cast<float>(head_dim) : 0.0f;
+    p.one2 = make_float2(1.0f, 1.0f);
+    p.mone2 = make_float2(-1.0f, -1.0f);
     // Packed rows [Q | K | V]; all three parts; one slot per part.
     p.in_part_off[0] = 0;
     p.in_part_off[1] = HD;

@@ -197,6 +197,8 @@ struct Params {
     const int32_t* valid_lens;   // per-item valid lengths (device), or null
     unsigned int* sat_counts;    // kCastCount: clipped-element counters (device); null otherwise
     float kv_scale;              // sage mode: factor of K (binary32 out) and V (binary16 out)
+    float2 one2;                 // {1, 1} and {-1, -1}: the unit factors of the packed sums
+    float2 mone2;                // (see fma2 below); read at run time, never constants
     int64_t pf_span;             // elements of an input row the call reads ([0, pf_span))
     int32_t hs_shift;            // sliced launches: log2 of the head slices per row group
     int32_t hs_heads;            // sliced launches: heads per slice
@@ -331,6 +333,67 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b)
     return d;
 }
 
+// Packed fused multiply-add, RN(a*b + c) per half.  With b = {1, 1} or
+// {-1, -1} (run-time values from the parameter block, which the code
+// generator cannot fold) it is a correctly rounded sum RN(c +- a) of an
+// already rounded product a: the code generator cannot merge the product
+// that feeds it into a multiply-add, because that product is the
+// multiplicand here, not an addend.  So a packed product followed by this
+// sum keeps both rounding points of the plain definition.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// Packed sum RN(a + b) per half, for operands that are not fresh products
+// (sums of the reduction tree).
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// A binary32 value rounded to the 16-bit type (nearest even), returned as
+// binary32.  bfloat16: one conversion that packs the rounded value above a
+// zero half, which is that value's binary32 bit pattern.
+template <bool BF16>
+__device__ __forceinline__ float round16f(float a)
+{
+    if constexpr (BF16) {
+        uint32_t d;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(a), "f"(0.0f));
+        return __uint_as_float(d);
+    } else {
+        return __half2float(__float2half_rn(a));
+    }
+}
+template <bool BF16>
+__device__ __forceinline__ float2 round16f2(float2 v)
+{
+    if constexpr (BF16) {
+        return make_float2(round16f<true>(v.x), round16f<true>(v.y));
+    } else {
+        __half2 h = __floats2half2_rn(v.x, v.y);
+        return __half22float2(h);
+    }
+}
+
 // Max of packed 16-bit magnitudes, NaN ignored (the other operand is kept).
 template <bool BF16>
 __device__ __forceinline__ uint32_t hmax2_abs(uint32_t m, uint32_t y)
@@ -422,6 +485,81 @@ __device__ __forceinline__ void qk_row(const uint4 (&raw)[CH], const float4* w, 
             const float rv = __fadd_rn(__fmul_rn(uv.x, sn[q][i]), __fmul_rn(uv.y, cs[q][i]));  // u s + v c
             y[q][i] = rot[q][i] ? round2<BF16>(ro, rv) : n;
         }
+    }
+}
+
+// The same head row for the e4m3 casts, computed on packed pairs.  Pair p
+// holds the lane's chunks 2p and 2p+1 (chunks c + 2p*LPR and c + (2p+1)*LPR
+// of the row) side by side, element k of each, so every packed operation
+// does the work of two chunks: the squares and their running sums (a packed
+// product, then the unit-factor sum of fma2), the in-lane level of the
+// halving tree, the two products of the norm, the 16-bit rounding, the
+// rotation (four packed products and two unit-factor sums per two pairs of
+// channels) and the product with the cast factor.  The rounding points are
+// those of qk_row followed by emit_e4m3, one for one.
+// w2 points at the lane's weights in pair layout: float2 {w(chunk 2p, k),
+// w(chunk 2p+1, k)} at [p*8 + k].  cs2/sn2 hold the pairs' cos/sin in the
+// same layout.  Returns the e4m3 codes of chunk q in code[q] (channels 0..7,
+// lowest byte first); with COUNT, the values of the chunks with act[q] set
+// whose scaled magnitude exceeds 448 are added to sat.
+template <bool BF16, int LPR, int CH, bool COUNT>
+__device__ __forceinline__ void qk_row_pairs_e4m3(const uint4 (&raw)[CH], const float2* w2,
+                                                  const float2 (&cs2)[CH / 2][4], const float2 (&sn2)[CH / 2][4],
+                                                  const bool (&rot)[CH][4], float inv_d, float eps, int D,
+                                                  float2 one2, float2 mone2, float2 f2, const bool (&act)[CH],
+                                                  uint2 (&code)[CH], unsigned int& sat)
+{
+    static_assert(CH == 2 || CH == 4, "pairs of chunks");
+    constexpr int NP = CH / 2;
+    float2 X[NP][8];
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 a = widen2<BF16>(word(raw[2 * p], i));
+            const float2 b = widen2<BF16>(word(raw[2 * p + 1], i));
+            X[p][2 * i] = make_float2(a.x, b.x);
+            X[p][2 * i + 1] = make_float2(a.y, b.y);
+        }
+    // Sum of squares of each chunk, channels left to right (two chunks per pair).
+    float2 A[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+        A[p] = mul2(X[p][0], X[p][0]);
+#pragma unroll
+        for (int k = 1; k < 8; ++k) A[p] = fma2(mul2(X[p][k], X[p][k]), one2, A[p]);
+    }
+    // In-lane levels of the halving tree: chunk q pairs with chunk q + CH/2.
+    if constexpr (NP == 2) A[0] = add2(A[0], A[1]);
+    float ss = __fadd_rn(A[0].x, A[0].y);
+#pragma unroll
+    for (int o = LPR / 2; o >= 1; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    const float ms = inv_d != 0.0f ? __fmul_rn(ss, inv_d) : __fdiv_rn(ss, static_cast<float>(D));
+    const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+    const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+        uint32_t c16[2][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 wp = reinterpret_cast<const float4*>(w2)[p * 4 + i];
+            const float2 u = round16f2<BF16>(mul2(mul2(X[p][2 * i], inv2), make_float2(wp.x, wp.y)));
+            const float2 v = round16f2<BF16>(mul2(mul2(X[p][2 * i + 1], inv2), make_float2(wp.z, wp.w)));
+            const float2 c = cs2[p][i], s = sn2[p][i];
+            const float2 ro = round16f2<BF16>(fma2(mul2(v, s), mone2, mul2(u, c)));  // u c - v s
+            const float2 rv = round16f2<BF16>(fma2(mul2(u, s), one2, mul2(v, c)));   // u s + v c
+            const float2 yu = make_float2(rot[2 * p][i] ? ro.x : u.x, rot[2 * p + 1][i] ? ro.y : u.y);
+            const float2 yv = make_float2(rot[2 * p][i] ? rv.x : v.x, rot[2 * p + 1][i] ? rv.y : v.y);
+            const float2 zu = mul2(yu, f2), zv = mul2(yv, f2);
+            c16[0][i] = e4m3x2(zu.x, zv.x);
+            c16[1][i] = e4m3x2(zu.y, zv.y);
+            if constexpr (COUNT)
+                sat += (act[2 * p] ? (fabsf(zu.x) > 448.0f) + (fabsf(zv.x) > 448.0f) : 0) +
+                       (act[2 * p + 1] ? (fabsf(zu.y) > 448.0f) + (fabsf(zv.y) > 448.0f) : 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            code[2 * p + j] = make_uint2(c16[j][0] | (c16[j][1] << 16), c16[j][2] | (c16[j][3] << 16));
     }
 }
 
@@ -661,6 +799,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     const int D = p.head_dim;
     constexpr bool kCastMode = MODE == kCast || MODE == kCastCount;
     constexpr bool count_sat = MODE == kCastCount;
+    // The casts compute their Q/K rows on packed pairs of chunks (qk_row_pairs).
+    constexpr bool kPairs = kCastMode && CH >= 2;
     const int64_t n_groups = (p.rows + TPW - 1) / TPW;
     // Work items: a row group, or (SLICED, for calls too small to fill the
     // GPU) one of 2^hs_shift slices of hs_heads heads of a row group.
@@ -697,14 +837,17 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
 
     // Norm weights of Q and K in shared memory, laid out per lane:
     // ws[part][c][q*8 + k] = weight of channel 8*(c + q*LPR) + k (zero past
-    // the head), so a lane reads its CH*8 weights as 2*CH float4.
+    // the head), so a lane reads its CH*8 weights as 2*CH float4.  The pair
+    // layout of the casts interleaves chunks 2p and 2p+1 instead:
+    // ws[part][c][p*16 + 2*k + j] = weight of channel k of chunk 2p+j.
     __shared__ __align__(16) float ws[2][LPR][CH * 8];
     for (int t = threadIdx.x; t < 2 * LPR * CH * 8; t += NT) {
         const int part = t / (LPR * CH * 8), cc = (t / (CH * 8)) % LPR, q = (t / 8) % CH, k = t % 8;
         const float* w = part == 0 ? p.wq : p.wk;
         const int chunk = cc + q * LPR;
         const bool used = part >= p.qk_first && part < p.qk_end;  // a V-only call has no weights
-        ws[part][cc][q * 8 + k] = used && chunk < p.chunks ? __ldg(w + 8 * chunk + k) : 0.0f;
+        const int at = kPairs ? (q / 2) * 16 + 2 * k + (q % 2) : q * 8 + k;
+        ws[part][cc][at] = used && chunk < p.chunks ? __ldg(w + 8 * chunk + k) : 0.0f;
     }
     __syncthreads();
     // Largest |weight| of this lane per part (the amax pass's row bound).
@@ -951,6 +1094,27 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                             if (!act[q]) continue;
                             const int64_t off = obase + h * p.out_hstride + 8 * q * LPR;
                             store_f32x8(yf[q], p.kv_scale, part == 1, static_cast<float*>(p.out[part]) + off);
+                        }
+                        continue;
+                    }
+                    if constexpr (kPairs) {
+                        float2 cs2[CH / 2][4], sn2[CH / 2][4];
+#pragma unroll
+                        for (int pp = 0; pp < CH / 2; ++pp)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                cs2[pp][i] = make_float2(cs[2 * pp][i], cs[2 * pp + 1][i]);
+                                sn2[pp][i] = make_float2(sn[2 * pp][i], sn[2 * pp + 1][i]);
+                            }
+                        uint2 code[CH];
+                        qk_row_pairs_e4m3<BF16, LPR, CH, count_sat>(
+                            rw, reinterpret_cast<const float2*>(&ws[part][c][0]), cs2, sn2, rot, p.inv_d, p.eps, D,
+                            p.one2, p.mone2, make_float2(fac[part], fac[part]), act, code, sat[part]);
+#pragma unroll
+                        for (int q = 0; q < CH; ++q) {
+                            if (!act[q]) continue;
+                            const int64_t off = obase + h * p.out_hstride + 8 * q * LPR;
+                            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out[part]) + off) = code[q];
                         }
                         continue;
                     }
