@@ -438,6 +438,69 @@ def large_configs(dev, peak: float, iters: int = 20):
     return rows
 
 
+def pass_rooflines(dev, peak: float, iters: int = 20):
+    """The two passes of the dynamic e4m3 call, each timed alone through the
+    split entry points (h3qk_amax, then h3qk_cast with that amax): the
+    65,280-token latent tile and the 104,080-row prefix, plus the prefix's
+    static-table cast.  CUDA events on the launching stream around each
+    launch, median of `iters` after 3 warm-ups, L2 flushed before each by a
+    256 MB write.  Algorithmic bytes per launch: amax reads 6*H*D per valid
+    token; cast reads 6*H*D and writes 3*H*D."""
+    import numpy as np
+    import torch
+
+    from video_vae_decoder_qkv_gb300 import amax as amax_pass
+    from video_vae_decoder_qkv_gb300 import cast as cast_pass
+    from video_vae_decoder_qkv_gb300 import prepare
+
+    rows = {}
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream(dev)
+    for spec in (W.LATENT_65K_E4M3, W.PREFIX_104K_DYNAMIC):
+        inp = W.generate(spec)
+        qkv = torch.from_numpy(inp.qkv.view(np.int16)).to(dev).view(torch.bfloat16)
+        wq, wk, pos = (torch.from_numpy(a).to(dev) for a in (inp.wq, inp.wk, inp.pos))
+        table = torch.from_numpy(inp.static_scales).to(dev)
+        shape = (spec.batch, spec.heads, spec.seq, spec.head_dim)
+        out = tuple(torch.empty(shape, dtype=torch.float8_e4m3fn, device=dev) for _ in range(3))
+        sc = torch.empty(3, device=dev)
+        am = torch.empty(3, device=dev)
+        kw = dict(heads=spec.heads, head_dim=spec.head_dim, rotary_dim=spec.rotary_dim, valid_len=spec.valid_len,
+                  n_axes=spec.n_axes, axis_dims=spec.axis_dims, stream=side)
+        n = spec.valid_rows() * spec.hd
+        calls = (("amax", lambda: amax_pass(qkv, wq, wk, pos, out=am, **kw), 6 * n),
+                 ("cast", lambda: cast_pass(qkv, wq, wk, pos, am, out=out, out_scales=sc, **kw), 9 * n))
+        if spec.name.startswith("prefix"):
+            calls += (("static_cast", lambda: prepare(qkv, wq, wk, pos, scale_mode="static", static_scales=table,
+                                                      out=out, out_scales=sc, **kw), 9 * n),)
+        try:
+            for name, fn, nbytes in calls:
+                ts = []
+                with torch.cuda.stream(side):
+                    for i in range(3 + iters):
+                        scratch.fill_(i & 0xFF)
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record(side)
+                        fn()
+                        b.record(side)
+                        b.synchronize()
+                        if i >= 3:
+                            ts.append(a.elapsed_time(b))
+                ms = statistics.median(ts)
+                gbs = nbytes / (ms / 1e3) / 1e9
+                rows[f"{spec.name.split('_')[0]}_{name}"] = {
+                    "kernel": f"qkprep_kernel<bf16, LPR=8, CH=2, {'amax' if name == 'amax' else 'cast'}>",
+                    "ms": ms, "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                    "algorithmic_bytes_per_launch": nbytes}
+        except Exception as e:  # noqa: BLE001 - report, do not fail the bench line
+            rows[f"{spec.name}_error"] = str(e)[:200]
+        del qkv, out
+        torch.cuda.empty_cache()
+    del scratch
+    torch.cuda.empty_cache()
+    return rows
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -551,6 +614,7 @@ def run_ours(args):
     e2e_max, e2e_bytes = reduce_max_sum(dist, e2e_s, step_bytes * E, dev)
 
     large = large_configs(dev, measured_peak()[0]) if not args.tokens else None
+    passes = pass_rooflines(dev, measured_peak()[0]) if not args.tokens else None
     variants = variant_ops(dev, stream, qkv, wq, wk, pos, common, spec16)
     extra = adjacent_ops(dev, stream) if not args.tokens else None
     small = small_calls(dev) if not args.tokens else None
@@ -597,6 +661,7 @@ def run_ours(args):
                          "achieved": ach16, "peak": peak, "unit": "GB/s", "frac": ach16 / peak,
                          "traffic": recorded_traffic(), "peak_source": peak_src,
                          "algorithmic_bytes_per_launch": bytes16},
+            "pass_rooflines": passes,
             "e2e": {"value": e2e_bytes / e2e_max / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": E, "api": "h3qk_prepare_host (host buffers, chunked copies overlapped with the kernels), both calls of the step"},
             "gpu_launches": launches,

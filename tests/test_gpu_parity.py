@@ -209,23 +209,28 @@ def test_static_degenerate_table():
         _check_full(spec, inp, q, k, v, sc, want, fill=CANARY8)
 
 
-def test_non_finite_inputs_do_not_trap():
+@pytest.mark.parametrize("dtype", [W.FP16, W.BF16])
+def test_non_finite_inputs_do_not_trap(dtype):
     """NaN and infinity in a few rows: the call succeeds, rows without them
-    match the oracle bit for bit, the others match up to NaN payloads."""
+    match the oracle bit for bit, the others match up to NaN payloads; the
+    amax leaves NaN out (one V NaN is the last value of its row)."""
     import torch
 
+    nan, pinf, ninf = (0x7E00, 0x7C00, 0xFC00) if dtype == W.FP16 else (0x7FC0, 0x7F80, 0xFF80)
     for kw in ({}, dict(out_kind=W.OUT_E4M3, scale_mode=W.SCALE_DYNAMIC)):
-        spec = BASE.with_(in_dtype=W.FP16, seed=3, **kw)
+        spec = BASE.with_(in_dtype=dtype, seed=3, **kw)
         inp = G.inputs(spec)
         qkv = inp.qkv.copy()
-        qkv[5, 7] = 0x7E00    # NaN in Q of head 0
-        qkv[9, 300] = 0x7C00  # +inf in K
-        qkv[11, 700] = 0xFC00  # -inf in V
+        qkv[5, 7] = nan       # NaN in Q of head 0
+        qkv[9, 300] = pinf    # +inf in K
+        qkv[11, 700] = ninf   # -inf in V
+        qkv[13, 3 * spec.hd - 1] = nan  # NaN in V
+        qkv[14, 2 * spec.hd + 9] = nan  # NaN in V
         bad = W.Inputs(spec, qkv, inp.wq, inp.wk, inp.pos, inp.static_scales)
         q, k, v, sc = G.gpu_prepare(bad, fill=None)
         torch.cuda.synchronize()
         want = G.oracle_full(bad)
-        kind = "e4m3" if spec.out_kind == W.OUT_E4M3 else "fp16"
+        kind = "e4m3" if spec.out_kind == W.OUT_E4M3 else ("fp16" if dtype == W.FP16 else "bf16")
         for name, g, w in zip("qkv", (q, k, v), want[:3]):
             G.assert_codes_equal(G.host_codes(g), w, f"non-finite {name}", nan_kind=kind)
         if sc is not None:

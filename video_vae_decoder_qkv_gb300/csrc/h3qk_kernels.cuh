@@ -69,6 +69,12 @@ constexpr int kWarpsPerBlock = 8;    // head_dim > 64; see Shape for head_dim <=
 #define H3QK_TUNE_SAGE 44204
 #endif
 
+// The amax pass's pairwise second bound (qk_pair_may_exceed) runs in the
+// instances whose warps hold at least this many token rows.
+#ifndef H3QK_AMAX_PAIR_MIN_TPW
+#define H3QK_AMAX_PAIR_MIN_TPW 1
+#endif
+
 // kCastCount is the cast that also counts clipped values (opts.sat_counts):
 // a separate instance, so that the plain cast carries no counter state.
 enum Mode : int { kOut16 = 0, kAmax = 1, kCast = 2, kSage = 3, kCastCount = 4 };
@@ -394,27 +400,33 @@ __device__ __forceinline__ float2 round16f2(float2 v)
     }
 }
 
-// Max of packed 16-bit magnitudes, NaN ignored (the other operand is kept).
-template <bool BF16>
-__device__ __forceinline__ uint32_t hmax2_abs(uint32_t m, uint32_t y)
-{
-    uint32_t a = y & 0x7fff7fffu;
-    uint32_t r;
-    if constexpr (BF16) {
-        __nv_bfloat162 v = __hmax2(*reinterpret_cast<__nv_bfloat162*>(&m), *reinterpret_cast<__nv_bfloat162*>(&a));
-        r = *reinterpret_cast<uint32_t*>(&v);
-    } else {
-        __half2 v = __hmax2(*reinterpret_cast<__half2*>(&m), *reinterpret_cast<__half2*>(&a));
-        r = *reinterpret_cast<uint32_t*>(&v);
-    }
-    return r;
-}
-
 template <bool BF16>
 __device__ __forceinline__ float hmax2_to_float(uint32_t m)
 {
     const float2 f = widen2<BF16>(m);
     return fmaxf(f.x, f.y);
+}
+
+// Running max of packed 16-bit magnitudes in one instruction: each half of
+// the result has magnitude max(|m|, |y|), NaN ignored (the other operand is
+// kept), and the xor of the two sign bits as its sign.  Read it through
+// hmax2x_to_float, which drops the signs.
+template <bool BF16>
+__device__ __forceinline__ uint32_t hmax2x(uint32_t m, uint32_t y)
+{
+    uint32_t r;
+    if constexpr (BF16) {
+        asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(y));
+    } else {
+        asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(y));
+    }
+    return r;
+}
+
+template <bool BF16>
+__device__ __forceinline__ float hmax2x_to_float(uint32_t m)
+{
+    return hmax2_to_float<BF16>(m & 0x7fff7fffu);
 }
 
 __device__ __forceinline__ uint32_t word(const uint4& v, int i)
@@ -488,27 +500,31 @@ __device__ __forceinline__ void qk_row(const uint4 (&raw)[CH], const float4* w, 
     }
 }
 
-// The same head row for the e4m3 casts, computed on packed pairs.  Pair p
+// The same head row for the e4m3 modes, computed on packed pairs.  Pair p
 // holds the lane's chunks 2p and 2p+1 (chunks c + 2p*LPR and c + (2p+1)*LPR
 // of the row) side by side, element k of each, so every packed operation
 // does the work of two chunks: the squares and their running sums (a packed
 // product, then the unit-factor sum of fma2), the in-lane level of the
-// halving tree, the two products of the norm, the 16-bit rounding, the
+// halving tree, the two products of the norm, the 16-bit rounding and the
 // rotation (four packed products and two unit-factor sums per two pairs of
-// channels) and the product with the cast factor.  The rounding points are
-// those of qk_row followed by emit_e4m3, one for one.
+// channels).  The rounding points are those of qk_row, one for one.
 // w2 points at the lane's weights in pair layout: float2 {w(chunk 2p, k),
 // w(chunk 2p+1, k)} at [p*8 + k].  cs2/sn2 hold the pairs' cos/sin in the
-// same layout.  Returns the e4m3 codes of chunk q in code[q] (channels 0..7,
-// lowest byte first); with COUNT, the values of the chunks with act[q] set
-// whose scaled magnitude exceeds 448 are added to sat.
-template <bool BF16, int LPR, int CH, bool COUNT>
-__device__ __forceinline__ void qk_row_pairs_e4m3(const uint4 (&raw)[CH], const float2* w2,
-                                                  const float2 (&cs2)[CH / 2][4], const float2 (&sn2)[CH / 2][4],
-                                                  const bool (&rot)[CH][4], float inv_d, float eps, int D,
-                                                  float2 one2, float2 mone2, float2 f2, const bool (&act)[CH],
-                                                  uint2 (&code)[CH], unsigned int& sat)
+// same layout.  For each pair p and rotary pair slot i, sink(p, i, yu, yv)
+// receives the results, already rounded to 16 bits and held as binary32:
+// yu = channel 2i, yv = channel 2i+1 of chunks 2p (.x) and 2p+1 (.y).
+// RM says which channels the rotation applies to (the same for every lane
+// of a call, so the caller picks it once): kRotAll, every channel (no
+// per-value choice); kRotFirst (two chunks per lane), every channel of the
+// lane's first chunk and, when rot1 is set, all of its second chunk (one
+// choice per value of the second chunk); kRotAny, per pair as rot says.
+enum RotMode : int { kRotAny = 0, kRotAll = 1, kRotFirst = 2 };
+template <bool BF16, int LPR, int CH, int RM, class Sink>
+__device__ __forceinline__ void qk_row_pairs(const uint4 (&raw)[CH], const float2* w2, const float2 (&cs2)[CH / 2][4],
+                                             const float2 (&sn2)[CH / 2][4], const bool (&rot)[CH][4], bool rot1,
+                                             float inv_d, float eps, int D, float2 one2, float2 mone2, Sink&& sink)
 {
+    static_assert(RM != kRotFirst || CH == 2, "kRotFirst: two chunks per lane");
     static_assert(CH == 2 || CH == 4, "pairs of chunks");
     constexpr int NP = CH / 2;
     float2 X[NP][8];
@@ -538,8 +554,7 @@ __device__ __forceinline__ void qk_row_pairs_e4m3(const uint4 (&raw)[CH], const 
     const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
     const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-    for (int p = 0; p < NP; ++p) {
-        uint32_t c16[2][4];
+    for (int p = 0; p < NP; ++p)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float4 wp = reinterpret_cast<const float4*>(w2)[p * 4 + i];
@@ -548,19 +563,58 @@ __device__ __forceinline__ void qk_row_pairs_e4m3(const uint4 (&raw)[CH], const 
             const float2 c = cs2[p][i], s = sn2[p][i];
             const float2 ro = round16f2<BF16>(fma2(mul2(v, s), mone2, mul2(u, c)));  // u c - v s
             const float2 rv = round16f2<BF16>(fma2(mul2(u, s), one2, mul2(v, c)));   // u s + v c
-            const float2 yu = make_float2(rot[2 * p][i] ? ro.x : u.x, rot[2 * p + 1][i] ? ro.y : u.y);
-            const float2 yv = make_float2(rot[2 * p][i] ? rv.x : v.x, rot[2 * p + 1][i] ? rv.y : v.y);
-            const float2 zu = mul2(yu, f2), zv = mul2(yv, f2);
-            c16[0][i] = e4m3x2(zu.x, zv.x);
-            c16[1][i] = e4m3x2(zu.y, zv.y);
-            if constexpr (COUNT)
-                sat += (act[2 * p] ? (fabsf(zu.x) > 448.0f) + (fabsf(zv.x) > 448.0f) : 0) +
-                       (act[2 * p + 1] ? (fabsf(zu.y) > 448.0f) + (fabsf(zv.y) > 448.0f) : 0);
+            if constexpr (RM == kRotAll) {
+                sink(p, i, ro, rv);
+            } else if constexpr (RM == kRotFirst) {
+                sink(p, i, make_float2(ro.x, rot1 ? ro.y : u.y), make_float2(rv.x, rot1 ? rv.y : v.y));
+            } else {
+                sink(p, i, make_float2(rot[2 * p][i] ? ro.x : u.x, rot[2 * p + 1][i] ? ro.y : u.y),
+                     make_float2(rot[2 * p][i] ? rv.x : v.x, rot[2 * p + 1][i] ? rv.y : v.y));
+            }
         }
+}
+
+// The cast of one Q/K head row on packed pairs: e4m3 codes of chunk q in
+// code[q] (channels 0..7, lowest byte first), from the results of
+// qk_row_pairs times the factor f2 (one rounded packed product).  With
+// COUNT, the values of the chunks with act[q] set whose scaled magnitude
+// exceeds 448 are added to sat.
+template <bool BF16, int LPR, int CH, bool COUNT, int RM>
+__device__ __forceinline__ void qk_row_pairs_e4m3(const uint4 (&raw)[CH], const float2* w2,
+                                                  const float2 (&cs2)[CH / 2][4], const float2 (&sn2)[CH / 2][4],
+                                                  const bool (&rot)[CH][4], bool rot1, float inv_d, float eps, int D,
+                                                  float2 one2, float2 mone2, float2 f2, const bool (&act)[CH],
+                                                  uint2 (&code)[CH], unsigned int& sat)
+{
+    uint32_t c16[CH][4];
+    qk_row_pairs<BF16, LPR, CH, RM>(raw, w2, cs2, sn2, rot, rot1, inv_d, eps, D, one2, mone2,
+                                [&](int p, int i, float2 yu, float2 yv) {
+                                    const float2 zu = mul2(yu, f2), zv = mul2(yv, f2);
+                                    c16[2 * p][i] = e4m3x2(zu.x, zv.x);
+                                    c16[2 * p + 1][i] = e4m3x2(zu.y, zv.y);
+                                    if constexpr (COUNT)
+                                        sat += (act[2 * p] ? (fabsf(zu.x) > 448.0f) + (fabsf(zv.x) > 448.0f) : 0) +
+                                               (act[2 * p + 1] ? (fabsf(zu.y) > 448.0f) + (fabsf(zv.y) > 448.0f)
+                                                               : 0);
+                                });
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
-            code[2 * p + j] = make_uint2(c16[j][0] | (c16[j][1] << 16), c16[j][2] | (c16[j][3] << 16));
-    }
+    for (int q = 0; q < CH; ++q) code[q] = make_uint2(c16[q][0] | (c16[q][1] << 16), c16[q][2] | (c16[q][3] << 16));
+}
+
+// The largest |y| over the chunks with act[q] set of one Q/K head row on
+// packed pairs (NaN ignored), folded into m (a non-negative binary32).
+template <bool BF16, int LPR, int CH, int RM>
+__device__ __forceinline__ float qk_row_pairs_amax(const uint4 (&raw)[CH], const float2* w2,
+                                                   const float2 (&cs2)[CH / 2][4], const float2 (&sn2)[CH / 2][4],
+                                                   const bool (&rot)[CH][4], bool rot1, float inv_d, float eps, int D,
+                                                   float2 one2, float2 mone2, const bool (&act)[CH], float m)
+{
+    qk_row_pairs<BF16, LPR, CH, RM>(raw, w2, cs2, sn2, rot, rot1, inv_d, eps, D, one2, mone2,
+                                [&](int p, int i, float2 yu, float2 yv) {
+                                    if (act[2 * p]) m = fmaxf(m, fmaxf(fabsf(yu.x), fabsf(yv.x)));
+                                    if (act[2 * p + 1]) m = fmaxf(m, fmaxf(fabsf(yu.y), fabsf(yv.y)));
+                                });
+    return m;
 }
 
 // The same head row for the sage outputs: every step stays binary32 (the
@@ -663,7 +717,7 @@ __device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, fl
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 uint32_t w = word(raw[q], i);
-                m2 = hmax2_abs<true>(m2, w);
+                m2 = hmax2x<true>(m2, w);
                 __nv_bfloat162 r = __hfma2(*reinterpret_cast<__nv_bfloat162*>(&w),
                                            *reinterpret_cast<__nv_bfloat162*>(&w),
                                            *reinterpret_cast<__nv_bfloat162*>(&acc));
@@ -678,7 +732,7 @@ __device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, fl
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t w = word(raw[q], i);
-                m2 = hmax2_abs<false>(m2, w);
+                m2 = hmax2x<false>(m2, w);
                 const float2 x = widen2<false>(w);
                 acc = __ffma2_rn(x, x, acc);
             }
@@ -692,7 +746,7 @@ __device__ __forceinline__ float qk_bound(const uint4 (&raw)[CH], float wmax, fl
     t_out = t;
     const float inv = rsqrtf(t);
     constexpr float kMargin = !BF16 ? 1.45f : (CH == 1 ? 1.45f : (CH == 2 ? 1.47f : 1.49f));
-    return kMargin * inv * hmax2_to_float<BF16>(m2) * wmax + 0x1p-23f;
+    return kMargin * inv * hmax2x_to_float<BF16>(m2) * wmax + 0x1p-23f;
 }
 
 // Second, tighter test of the early-out, for rows whose first bound did not
@@ -744,6 +798,31 @@ __device__ __forceinline__ bool qk_pair_may_exceed(const uint4 (&raw)[CH], const
     return !(lhs < 0x1p127f && lhs <= known * known * t);
 }
 
+// qk_pair_may_exceed for the weights in pair layout (float2 {w(chunk 2p, k),
+// w(chunk 2p+1, k)} at [p*8 + k]): the same pair squares, two chunks per
+// packed operation.
+template <bool BF16, int CH>
+__device__ __forceinline__ bool qk_pair_may_exceed2(const uint4 (&raw)[CH], const float2* w2, float t, float known)
+{
+    float m = 0.0f;
+#pragma unroll
+    for (int p = 0; p < CH / 2; ++p)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 wp = reinterpret_cast<const float4*>(w2)[p * 4 + i];
+            const float2 a = widen2<BF16>(word(raw[2 * p], i));
+            const float2 b = widen2<BF16>(word(raw[2 * p + 1], i));
+            const float2 zu = mul2(make_float2(a.x, b.x), make_float2(wp.x, wp.y));
+            const float2 zv = mul2(make_float2(a.y, b.y), make_float2(wp.z, wp.w));
+            const float2 sq = fma2(zu, zu, mul2(zv, zv));
+            m = fmax_keep_nan(m, fmax_keep_nan(sq.x, sq.y));
+        }
+    if (!(known >= 0x1p-13f && known <= 0x1p60f)) return true;
+    constexpr float kK2 = !BF16 ? 1.01f : (CH == 1 ? 1.04f : (CH == 2 ? 1.06f : 1.09f));
+    const float lhs = kK2 * m;
+    return !(lhs < 0x1p127f && lhs <= known * known * t);
+}
+
 // Eight 16-bit values -> eight e4m3 codes at dst (8 bytes); with COUNT, adds
 // the number of values whose scaled magnitude exceeds 448 (clipped to the
 // largest code) to sat.
@@ -779,7 +858,7 @@ __device__ __forceinline__ void emit_e4m3(const uint32_t (&y)[4], float f, uint8
 // kCastCount does the same and adds the clipped-value counts; kSage writes
 // binary32 Q, binary32 K * kv_scale and binary16 V * kv_scale.
 // ---------------------------------------------------------------------------
-template <bool BF16, int LPR, int CH, int MODE, bool SLICED>
+template <bool BF16, int LPR, int CH, int MODE, bool SLICED, int RM>
 __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     qkprep_kernel(const __grid_constant__ Params p)
 {
@@ -799,8 +878,13 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     const int D = p.head_dim;
     constexpr bool kCastMode = MODE == kCast || MODE == kCastCount;
     constexpr bool count_sat = MODE == kCastCount;
-    // The casts compute their Q/K rows on packed pairs of chunks (qk_row_pairs).
-    constexpr bool kPairs = kCastMode && CH >= 2;
+    // The e4m3 modes compute their Q/K rows on packed pairs of chunks (qk_row_pairs).
+    constexpr bool kPairs = (kCastMode || MODE == kAmax) && CH >= 2;
+    // Which channels rotate is a property of the call (RM, a RotMode chosen
+    // at launch by rot_mode_of): all of them; the first chunk of every lane
+    // and the second chunk of the lanes where rot1 is set; or any pattern.
+    static_assert(RM == kRotAny || kPairs, "rotation modes other than kRotAny: e4m3 pair instances only");
+    const bool rot1 = CH == 2 && 8 * (c + LPR) + 8 <= p.rotary_dim;
     const int64_t n_groups = (p.rows + TPW - 1) / TPW;
     // Work items: a row group, or (SLICED, for calls too small to fill the
     // GPU) one of 2^hs_shift slices of hs_heads heads of a row group.
@@ -867,7 +951,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     uint32_t pub[2] = {0u, 0u};
     uint32_t thr[2] = {0u, 0u};
 
-    uint32_t am[3] = {0u, 0u, 0u};  // packed 16-bit running max of |y| per tensor
+    uint32_t am[3] = {0u, 0u, 0u};  // packed 16-bit running max of |y| per tensor (hmax2x)
+    float amf[2] = {0.0f, 0.0f};    // pair path: running max of |y| of Q and K
     unsigned int sat[3] = {0u, 0u, 0u};
 
     // ---- shared-memory pipeline (S > 0) -------------------------------------
@@ -1068,16 +1153,20 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                         const uint32_t bb = act_row ? __float_as_uint(bnd) : 0u;
                         const uint32_t known = run[part] > thr[part] ? run[part] : thr[part];
                         if (__reduce_max_sync(0xffffffffu, bb) <= known) continue;  // warp-uniform
-                        if constexpr (TPW >= 8) {
-                            // The vote spans 8 or more token rows here, so the
-                            // first bound fails often (about half the Q head rows
-                            // at head_dim 64), and the pairwise test pays for
-                            // itself; with 4 rows per warp it costs more than it
-                            // saves.
-                            const bool may = act_row && (!(bnd < 0x1p127f) ||
-                                                         qk_pair_may_exceed<BF16, CH>(
-                                                             rw, reinterpret_cast<const float4*>(&ws[part][c][0]), t,
-                                                             __uint_as_float(known)));
+                        if constexpr (TPW >= H3QK_AMAX_PAIR_MIN_TPW) {
+                            // Where the first vote fails (a head with an outlier
+                            // channel fails it in every row), the pairwise test
+                            // lets most rows skip the exact path.
+                            bool may = act_row && !(bnd < 0x1p127f);
+                            if constexpr (kPairs) {
+                                may = may || (act_row && qk_pair_may_exceed2<BF16, CH>(
+                                                             rw, reinterpret_cast<const float2*>(&ws[part][c][0]),
+                                                             t, __uint_as_float(known)));
+                            } else {
+                                may = may || (act_row && qk_pair_may_exceed<BF16, CH>(
+                                                             rw, reinterpret_cast<const float4*>(&ws[part][c][0]),
+                                                             t, __uint_as_float(known)));
+                            }
                             if (!__any_sync(0xffffffffu, may)) continue;  // warp-uniform
                         }
                         if (!have_angles) {
@@ -1097,7 +1186,25 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                         }
                         continue;
                     }
-                    if constexpr (kPairs) {
+                    if constexpr (kPairs && MODE == kAmax) {
+                        float2 cs2[CH / 2][4], sn2[CH / 2][4];
+#pragma unroll
+                        for (int pp = 0; pp < CH / 2; ++pp)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                cs2[pp][i] = make_float2(cs[2 * pp][i], cs[2 * pp + 1][i]);
+                                sn2[pp][i] = make_float2(sn[2 * pp][i], sn[2 * pp + 1][i]);
+                            }
+                        amf[part] = qk_row_pairs_amax<BF16, LPR, CH, RM>(
+                            rw, reinterpret_cast<const float2*>(&ws[part][c][0]), cs2, sn2, rot, rot1, p.inv_d,
+                            p.eps, D, p.one2, p.mone2, act, amf[part]);
+                        run[part] = __reduce_max_sync(0xffffffffu, __float_as_uint(amf[part]));
+                        if (run[part] > pub[part]) {  // warp-uniform
+                            if (lane == 0) atomicMax(p.amax_words + p.slot[part], run[part]);
+                            pub[part] = run[part];
+                        }
+                        continue;
+                    } else if constexpr (kPairs) {
                         float2 cs2[CH / 2][4], sn2[CH / 2][4];
 #pragma unroll
                         for (int pp = 0; pp < CH / 2; ++pp)
@@ -1107,9 +1214,9 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                                 sn2[pp][i] = make_float2(sn[2 * pp][i], sn[2 * pp + 1][i]);
                             }
                         uint2 code[CH];
-                        qk_row_pairs_e4m3<BF16, LPR, CH, count_sat>(
-                            rw, reinterpret_cast<const float2*>(&ws[part][c][0]), cs2, sn2, rot, p.inv_d, p.eps, D,
-                            p.one2, p.mone2, make_float2(fac[part], fac[part]), act, code, sat[part]);
+                        qk_row_pairs_e4m3<BF16, LPR, CH, count_sat, RM>(
+                            rw, reinterpret_cast<const float2*>(&ws[part][c][0]), cs2, sn2, rot, rot1, p.inv_d,
+                            p.eps, D, p.one2, p.mone2, make_float2(fac[part], fac[part]), act, code, sat[part]);
 #pragma unroll
                         for (int q = 0; q < CH; ++q) {
                             if (!act[q]) continue;
@@ -1130,14 +1237,14 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                             *reinterpret_cast<uint4*>(dst) = make_uint4(y[q][0], y[q][1], y[q][2], y[q][3]);
                         } else if constexpr (MODE == kAmax) {
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) am[part] = hmax2_abs<BF16>(am[part], y[q][i]);
+                            for (int i = 0; i < 4; ++i) am[part] = hmax2x<BF16>(am[part], y[q][i]);
                         } else {
                             uint8_t* dst = static_cast<uint8_t*>(p.out[part]) + off;
                             emit_e4m3<BF16, count_sat>(y[q], fac[part], dst, sat[part]);
                         }
                     }
                     if constexpr (MODE == kAmax) {
-                        run[part] = __reduce_max_sync(0xffffffffu, __float_as_uint(hmax2_to_float<BF16>(am[part])));
+                        run[part] = __reduce_max_sync(0xffffffffu, __float_as_uint(hmax2x_to_float<BF16>(am[part])));
                         if (run[part] > pub[part]) {  // warp-uniform
                             if (lane == 0) atomicMax(p.amax_words + p.slot[part], run[part]);
                             pub[part] = run[part];
@@ -1188,7 +1295,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                             store_v_f16<BF16>(raw[u][q], p.kv_scale, static_cast<uint16_t*>(p.out[2]) + off);
                         } else if constexpr (MODE == kAmax) {
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) am[2] = hmax2_abs<BF16>(am[2], word(raw[u][q], i));
+                            for (int i = 0; i < 4; ++i) am[2] = hmax2x<BF16>(am[2], word(raw[u][q], i));
                         } else {
                             const uint32_t yv[4] = {raw[u][q].x, raw[u][q].y, raw[u][q].z, raw[u][q].w};
                             uint8_t* dst = static_cast<uint8_t*>(p.out[2]) + off;
@@ -1206,7 +1313,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
         __shared__ float red[3][Shape<MODE, LPR>::W];
 #pragma unroll
         for (int t = 0; t < 3; ++t) {
-            float m = hmax2_to_float<BF16>(am[t]);
+            float m = hmax2x_to_float<BF16>(am[t]);
+            if (kPairs && t < 2) m = amf[t];
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
             if (lane == 0) red[t][threadIdx.x >> 5] = m;
@@ -1231,5 +1339,15 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     }
 }
 
+
+// The rotation mode (RotMode) of a call with rotary width R and head_dim D
+// on an instance with LPR lanes and CH chunks per lane: every channel
+// rotates (R == D); every lane's first chunk rotates and second chunks rotate
+// whole or not at all (two chunks per lane, R a multiple of 8 covering the
+// first LPR chunks); else any pattern.
+__host__ __device__ constexpr int rot_mode_of(int R, int D, int LPR, int CH)
+{
+    return R == D ? kRotAll : ((CH == 2 && R % 8 == 0 && R >= 8 * LPR) ? kRotFirst : kRotAny);
+}
 
 }  // namespace h3qk

@@ -55,14 +55,14 @@ constexpr int waves()
 // take dynamic shared memory; the kernel's dynamic limit is raised to that
 // size once per device (static and dynamic together may exceed the 48 KB
 // default).
-template <bool BF16, int LPR, int CH, int MODE, bool SLICED>
+template <bool BF16, int LPR, int CH, int MODE, bool SLICED, int RM>
 cudaError_t launch_sliced(const h3qk::Params& p, cudaStream_t st)
 {
     constexpr size_t smem = h3qk::stage_bytes<LPR, CH, MODE>();
     static_assert(smem <= 227 * 1024, "a block's pipeline stages exceed the 227 KB of shared memory per block");
     constexpr int W = h3qk::Shape<MODE, LPR>::W;
     constexpr int NT = h3qk::Shape<MODE, LPR>::NT;
-    auto* kernel = h3qk::qkprep_kernel<BF16, LPR, CH, MODE, SLICED>;
+    auto* kernel = h3qk::qkprep_kernel<BF16, LPR, CH, MODE, SLICED, RM>;
     if constexpr (smem > 0) {
         static std::mutex mu;
         static bool raised[kMaxDevices] = {false};
@@ -103,6 +103,25 @@ cudaError_t launch_sliced(const h3qk::Params& p, cudaStream_t st)
 // each group's heads into 2^shift slices of at least 2 heads (no slice
 // empty: the copy pipeline walks one batch sequence per slice and part) and
 // runs the sliced kernel; every other call runs the plain kernel.
+// The instance for the call's rotation mode: the e4m3 modes on pairs of
+// chunks have one per RotMode (rotation choices fixed at compile time), the
+// other modes only the general one.
+template <bool BF16, int LPR, int CH, int MODE, bool SLICED>
+cudaError_t launch_rm(const h3qk::Params& p, cudaStream_t st)
+{
+    constexpr bool pairs = (MODE == h3qk::kAmax || MODE == h3qk::kCast || MODE == h3qk::kCastCount) && CH >= 2;
+    if constexpr (pairs) {
+        switch (h3qk::rot_mode_of(p.rotary_dim, p.head_dim, LPR, CH)) {
+        case h3qk::kRotAll: return launch_sliced<BF16, LPR, CH, MODE, SLICED, h3qk::kRotAll>(p, st);
+        case h3qk::kRotFirst:
+            if constexpr (CH == 2) return launch_sliced<BF16, LPR, CH, MODE, SLICED, h3qk::kRotFirst>(p, st);
+            break;
+        default: break;
+        }
+    }
+    return launch_sliced<BF16, LPR, CH, MODE, SLICED, h3qk::kRotAny>(p, st);
+}
+
 template <bool BF16, int LPR, int CH, int MODE>
 cudaError_t launch_one(const h3qk::Params& p0, cudaStream_t st)
 {
@@ -117,11 +136,11 @@ cudaError_t launch_one(const h3qk::Params& p0, cudaStream_t st)
         --shift;
         per = (heads + (1 << shift) - 1) >> shift;
     }
-    if (shift == 0) return launch_sliced<BF16, LPR, CH, MODE, false>(p0, st);
+    if (shift == 0) return launch_rm<BF16, LPR, CH, MODE, false>(p0, st);
     h3qk::Params p = p0;
     p.hs_shift = shift;
     p.hs_heads = per;
-    return launch_sliced<BF16, LPR, CH, MODE, true>(p, st);
+    return launch_rm<BF16, LPR, CH, MODE, true>(p, st);
 }
 
 // P = next_pow2(D/8) chunk slots per head row: the mode's CH per lane on
