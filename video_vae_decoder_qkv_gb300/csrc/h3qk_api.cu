@@ -21,6 +21,9 @@ namespace h3qk {
 // the one translation unit that launches it).
 __global__ void amax_init_kernel(unsigned int* words)
 {
+    // The amax pass that follows is a chained launch (it waits for this
+    // kernel to complete before it reads the words).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x < 3) words[threadIdx.x] = 0u;
 }
 
@@ -280,7 +283,9 @@ h3qk_status run_amax(const Plan& pl)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e);
     if (pl.p.rows > 0 && (pl.p.valid_len > 0 || pl.p.valid_lens)) {
-        e = launch(pl.bf16, pl.P, h3qk::kAmax, pl.p, pl.st);
+        h3qk::Params pa = pl.p;
+        pa.chained = 1;  // a programmatic dependent of the zeroing kernel
+        e = launch(pl.bf16, pl.P, h3qk::kAmax, pa, pl.st);
         if (e != cudaSuccess) return fail_cuda(e);
     }
     return H3QK_OK;
@@ -365,6 +370,7 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
     if (scale_mode == H3QK_SCALE_DYNAMIC) {
         s = run_amax(pl);
         if (s != H3QK_OK) return s;
+        p.chained = 1;  // a programmatic dependent of the amax pass
     }
     e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.st);
     return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
@@ -463,6 +469,7 @@ h3qk_status h3qk_norm_rope_tensor(const void* x, const float* norm_w, const int3
     if (scale_mode == H3QK_SCALE_DYNAMIC) {
         s = run_amax(pl);
         if (s != H3QK_OK) return s;
+        p.chained = 1;  // a programmatic dependent of the amax pass
     }
     e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.st);
     return e == cudaSuccess ? H3QK_OK : fail_cuda(e);

@@ -203,6 +203,8 @@ struct Params {
     const int32_t* valid_lens;   // per-item valid lengths (device), or null
     unsigned int* sat_counts;    // kCastCount: clipped-element counters (device); null otherwise
     float kv_scale;              // sage mode: factor of K (binary32 out) and V (binary16 out)
+    int32_t chained;             // host only: launched as a programmatic dependent of the
+                                 // call's previous kernel (see the griddepcontrol notes)
     float2 one2;                 // {1, 1} and {-1, -1}: the unit factors of the packed sums
     float2 mone2;                // (see fma2 below); read at run time, never constants
     int64_t pf_span;             // elements of an input row the call reads ([0, pf_span))
@@ -895,29 +897,20 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * NT + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * NT) >> 5;
 
-    // Cast factors (each thread derives them; block 0 publishes the descales).
-    float fac[3] = {1.0f, 1.0f, 1.0f};
-    if constexpr (kCastMode) {
-#pragma unroll
-        for (int t = 0; t < 3; ++t) {
-            if (p.slot[t] < 0) continue;
-            // One load from whichever table this mode uses (never a NULL pointer).
-            const float a = __uint_as_float(__ldcg(p.scale_words + p.slot[t]));
-            const bool ok = a >= 1.17549435e-38f && a <= 3.40282347e+38f;
-            float s = 1.0f, f = 1.0f;
-            if (ok) {
-                if (p.dynamic) {
-                    s = __fdiv_rn(a, 448.0f);
-                    f = __fdiv_rn(448.0f, a);
-                } else {
-                    s = a;
-                    f = __frcp_rn(a);
-                }
-            }
-            fac[t] = f;
-            if (blockIdx.x == 0 && threadIdx.x == 0) p.out_scales[p.slot[t]] = s;
-        }
-    }
+    // Chained launches.  A dynamic call runs three kernels: zero the amax
+    // words, the amax pass, the cast.  The second and third are launched as
+    // programmatic dependents of the one before (griddepcontrol), so each
+    // is scheduled while its predecessor drains and stages its weights and
+    // its first input copies meanwhile; it waits for the predecessor to
+    // complete, with its writes visible, before it touches the amax words
+    // (the amax pass before its first read of them, the cast before it
+    // derives its factors).  Nothing before the wait reads or writes memory
+    // that the predecessor writes, and the first kernel of a call is never
+    // chained, so the inputs are complete when any kernel of the call
+    // starts.  Outside a chained launch the wait returns at once.  The amax
+    // pass lets its dependent (the cast) be scheduled from its start: the
+    // cast's blocks only take SM room that finished amax blocks leave.
+    if constexpr (MODE == kAmax) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // Norm weights of Q and K in shared memory, laid out per lane:
     // ws[part][c][q*8 + k] = weight of channel 8*(c + q*LPR) + k (zero past
@@ -1024,6 +1017,33 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
         if (fit < n_items) feed_group();
 #pragma unroll 1
         for (int k = 0; k < S - 1; ++k) issue();
+    }
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // Cast factors (each thread derives them; block 0 publishes the descales),
+    // read after the wait above.
+    float fac[3] = {1.0f, 1.0f, 1.0f};
+    if constexpr (kCastMode) {
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+            if (p.slot[t] < 0) continue;
+            // One load from whichever table this mode uses (never a NULL pointer).
+            const float a = __uint_as_float(__ldcg(p.scale_words + p.slot[t]));
+            const bool ok = a >= 1.17549435e-38f && a <= 3.40282347e+38f;
+            float s = 1.0f, f = 1.0f;
+            if (ok) {
+                if (p.dynamic) {
+                    s = __fdiv_rn(a, 448.0f);
+                    f = __fdiv_rn(448.0f, a);
+                } else {
+                    s = a;
+                    f = __frcp_rn(a);
+                }
+            }
+            fac[t] = f;
+            if (blockIdx.x == 0 && threadIdx.x == 0) p.out_scales[p.slot[t]] = s;
+        }
     }
 
     for (int64_t it = warp0; it < n_items; it += n_warps) {

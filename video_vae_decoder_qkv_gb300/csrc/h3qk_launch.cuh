@@ -94,6 +94,24 @@ cudaError_t launch_sliced(const h3qk::Params& p, cudaStream_t st)
         cap = static_cast<int64_t>(h3qk_internal_sm_count()) * occ[dev] * waves<MODE>();
     }
     const int blocks = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
+    if (p.chained) {
+        // A programmatic dependent of the previous kernel on the stream: it
+        // may be scheduled before that kernel completes and waits for it
+        // (griddepcontrol.wait) before touching what it writes.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+        cfg.blockDim = dim3(NT);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+        h3qk_internal_count_launch();
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     kernel<<<blocks, NT, smem, st>>>(p);
     h3qk_internal_count_launch();
     return cudaGetLastError();
