@@ -166,9 +166,10 @@ def kernel_sha() -> str:
     return h.hexdigest()
 
 
-def recorded_traffic():
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None when the kernel source changed since the capture."""
+def recorded_traffic(key: str = "out16_latent65k"):
+    """DRAM bytes (read + write) per launch of one kernel on one workload from
+    the committed ncu record (profiles/traffic.json), or None when the kernel
+    source changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -177,7 +178,8 @@ def recorded_traffic():
         return None
     if rec.get("kernel_source_sha256") != kernel_sha():
         return None
-    return rec.get("dram_bytes_per_launch")
+    k = rec.get("kernels", {}).get(key)
+    return k.get("dram_bytes_per_launch") if k else None
 
 
 # --------------------------------------------------------------------------
@@ -488,10 +490,13 @@ def pass_rooflines(dev, peak: float, iters: int = 20):
                             ts.append(a.elapsed_time(b))
                 ms = statistics.median(ts)
                 gbs = nbytes / (ms / 1e3) / 1e9
-                rows[f"{spec.name.split('_')[0]}_{name}"] = {
+                tag = spec.name.split("_")[0]
+                key = {"latent": "latent65k", "prefix": "prefix104k"}[tag]
+                rows[f"{tag}_{name}"] = {
                     "kernel": f"qkprep_kernel<bf16, LPR=8, CH=2, {'amax' if name == 'amax' else 'cast'}>",
                     "ms": ms, "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                    "algorithmic_bytes_per_launch": nbytes}
+                    "algorithmic_bytes_per_launch": nbytes,
+                    "traffic": recorded_traffic(f"{name}_{key}")}
         except Exception as e:  # noqa: BLE001 - report, do not fail the bench line
             rows[f"{spec.name}_error"] = str(e)[:200]
         del qkv, out
