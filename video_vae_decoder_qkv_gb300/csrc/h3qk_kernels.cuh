@@ -69,6 +69,13 @@ constexpr int kWarpsPerBlock = 8;    // head_dim > 64; see Shape for head_dim <=
 #define H3QK_TUNE_SAGE 44204
 #endif
 
+// kRotFirst instances (see RotMode) are used from this many lanes per head
+// row up; narrower heads take the general instance (at head_dim 64 the
+// kRotFirst cast spills and measured 10 % slower).
+#ifndef H3QK_ROT_FIRST_MIN_LPR
+#define H3QK_ROT_FIRST_MIN_LPR 8
+#endif
+
 // The amax pass's pairwise second bound (qk_pair_may_exceed) runs in the
 // instances whose warps hold at least this many token rows.
 #ifndef H3QK_AMAX_PAIR_MIN_TPW
@@ -1367,7 +1374,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
 // first LPR chunks); else any pattern.
 __host__ __device__ constexpr int rot_mode_of(int R, int D, int LPR, int CH)
 {
-    return R == D ? kRotAll : ((CH == 2 && R % 8 == 0 && R >= 8 * LPR) ? kRotFirst : kRotAny);
+    return R == D ? kRotAll
+                  : ((CH == 2 && LPR >= H3QK_ROT_FIRST_MIN_LPR && R % 8 == 0 && R >= 8 * LPR) ? kRotFirst : kRotAny);
 }
 
 }  // namespace h3qk
