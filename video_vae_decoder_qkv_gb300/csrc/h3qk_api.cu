@@ -371,6 +371,7 @@ h3qk_status h3qk_prepare(const void* qkv, const float* norm_wq, const float* nor
         s = run_amax(pl);
         if (s != H3QK_OK) return s;
         p.chained = 1;  // a programmatic dependent of the amax pass
+        p.reverse = 1;  // starts with the rows the amax pass read last (in L2)
     }
     e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.st);
     return e == cudaSuccess ? H3QK_OK : fail_cuda(e);
@@ -470,6 +471,7 @@ h3qk_status h3qk_norm_rope_tensor(const void* x, const float* norm_w, const int3
         s = run_amax(pl);
         if (s != H3QK_OK) return s;
         p.chained = 1;  // a programmatic dependent of the amax pass
+        p.reverse = 1;  // starts with the rows the amax pass read last (in L2)
     }
     e = launch(pl.bf16, pl.P, h3qk::kCast, p, pl.st);
     return e == cudaSuccess ? H3QK_OK : fail_cuda(e);

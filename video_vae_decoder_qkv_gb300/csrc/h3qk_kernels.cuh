@@ -212,6 +212,8 @@ struct Params {
     float kv_scale;              // sage mode: factor of K (binary32 out) and V (binary16 out)
     int32_t chained;             // host only: launched as a programmatic dependent of the
                                  // call's previous kernel (see the griddepcontrol notes)
+    int32_t reverse;             // walk the row groups from the last one down (the cast
+                                 // after an amax pass: see the note in the kernel)
     float2 one2;                 // {1, 1} and {-1, -1}: the unit factors of the packed sums
     float2 mone2;                // (see fma2 below); read at run time, never constants
     int64_t pf_span;             // elements of an input row the call reads ([0, pf_span))
@@ -900,6 +902,15 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     const int hs_shift = SLICED ? p.hs_shift : 0;
     const int64_t n_items = n_groups << hs_shift;
     const int hs_mask = (1 << hs_shift) - 1;
+    // Row group of work item it.  The cast of a dynamic call walks the groups
+    // from the last one down: its amax pass (the kernel just before it, which
+    // only reads) walked them upwards, so the input rows it read last are
+    // still in L2 and the cast reads those first.
+    const bool rev = kCastMode && p.reverse != 0;
+    auto group_of = [&](int64_t item) {
+        const int64_t g0 = item >> hs_shift;
+        return rev ? n_groups - 1 - g0 : g0;
+    };
     constexpr int NT = Shape<MODE, LPR>::NT;  // threads per block
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * NT + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * NT) >> 5;
@@ -973,7 +984,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
             fh_hi = min(H, fh_lo + p.hs_heads);
             fh0 = fh_lo;
         }
-        const int64_t rr = (fit >> hs_shift) * TPW + sub;
+        const int64_t rr = group_of(fit) * TPW + sub;
         bool ok = false;
         if (rr < p.rows) {
             const int64_t bb = rr / p.seq;
@@ -1054,7 +1065,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     }
 
     for (int64_t it = warp0; it < n_items; it += n_warps) {
-        const int64_t g = it >> hs_shift;
+        const int64_t g = group_of(it);
         const int h_lo = SLICED ? static_cast<int>(it & hs_mask) * p.hs_heads : 0;
         const int h_hi = SLICED ? min(H, h_lo + p.hs_heads) : H;
         const int64_t r = g * TPW + sub;
@@ -1115,9 +1126,9 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                 int64_t rr = r;
                 if (off >= p.pf_span) {
                     off -= p.pf_span;
-                    rr = ((it + n_warps) >> hs_shift) * TPW + sub;
+                    rr = group_of(it + n_warps) * TPW + sub;
                 }
-                if (rr >= p.rows || off >= p.pf_span) return;
+                if (rr < 0 || rr >= p.rows || off >= p.pf_span) return;  // past the last item either way
                 if (off + n > p.pf_span) n = p.pf_span - off;
                 prefetch_l2(p.qkv + rr * p.row_stride + off, static_cast<uint32_t>(2 * n));
             }
