@@ -289,7 +289,8 @@ h3qk_status h3qk_prepare_sage(const void* qkv, const float* norm_wq, const float
  * entry adds the transfers for callers whose tensors live on the host, the
  * whole round trip being one library call.
  *
- * The call is cut into chunks of at most 8,192 token rows inside one item.
+ * The call is cut into chunks of about 64 MiB of input rows (256 to 8,192
+ * token rows) inside one item.
  * Three streams owned by the library (created on the first call on each
  * device) copy a chunk in, compute it and copy it out, so the transfers of
  * one chunk overlap the kernels and transfers of others.  In dynamic e4m3

@@ -11,7 +11,8 @@
 using namespace h3qk_detail;
 
 // h3qk_prepare_host: the path on host buffers.  The call is cut into chunks
-// of at most kHostChunkRows token rows inside one item; three streams of the
+// of about H3QK_HOST_CHUNK_BYTES of input rows (chunk_rows below) inside one
+// item; three streams of the
 // library (host -> device copies, kernels, device -> host copies) keep the
 // copies of one chunk in flight while another computes.  Device memory comes
 // from the caller's workspace: a ring of kHostSlots chunk slots (or, for
@@ -20,8 +21,25 @@ using namespace h3qk_detail;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int64_t kHostChunkRows = 8192;
 constexpr int kHostSlots = 3;
+
+// Input bytes per chunk.  Smaller chunks shorten the pipeline's fill (the
+// first chunk's copy in) and drain (the last chunk's copy out), larger ones
+// pay the per-copy cost less often.  On the 65k tile's two calls (GB300) the
+// step took 17.7 ms at 8,192-row chunks (151 MB), 17.3 ms at 64 MiB, 17.9 ms
+// at 32 MiB, 18.3 ms at 16 MiB and 19.8 ms at 8 MiB.
+#ifndef H3QK_HOST_CHUNK_BYTES
+#define H3QK_HOST_CHUNK_BYTES (64 << 20)
+#endif
+
+// Rows per chunk: H3QK_HOST_CHUNK_BYTES of input rows, between 256 and
+// 8,192 rows, never more than the rows of one item.
+int64_t chunk_rows(int64_t seq, int64_t stride)
+{
+    int64_t n = static_cast<int64_t>(H3QK_HOST_CHUNK_BYTES) / (stride * 2);
+    n = n < 256 ? 256 : (n > 8192 ? 8192 : n);
+    return seq < n ? seq : n;
+}
 
 struct HostStreams {
     std::mutex call;                                   // one host call enqueues at a time
@@ -84,7 +102,7 @@ HostLayout host_layout(int64_t tokens, int64_t seq, int32_t heads, int32_t head_
 {
     HostLayout L;
     const int64_t HD = static_cast<int64_t>(heads) * head_dim;
-    L.chunk = seq < kHostChunkRows ? seq : kHostChunkRows;
+    L.chunk = chunk_rows(seq, stride);
     size_t off = 0;
     L.w = off;
     off += round256(2 * static_cast<size_t>(head_dim) * 4);
