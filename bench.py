@@ -292,9 +292,11 @@ def adjacent_ops(dev, stream, iters: int = 20):
 
 def variant_ops(dev, stream, qkv, wq, wk, pos, common, spec, iters: int = 20):
     """Other output forms of the path on the same tile, timed after the main
-    region: the sage outputs (float32 Q, float32 K * kv_scale, float16 V *
-    kv_scale; 6 bytes read + 10 written per element) and the e4m3 cast with
-    a static scale table (6 read + 3 written)."""
+    region the way `large_configs` times its calls: the sage outputs (float32
+    Q, float32 K * kv_scale, float16 V * kv_scale; 6 bytes read + 10 written
+    per element) and the e4m3 cast with a static scale table (6 read + 3
+    written).  CUDA events around each call on its stream, median of `iters`
+    after 3 warm-ups, L2 flushed before each call by a 256 MB write."""
     import torch
 
     from video_vae_decoder_qkv_gb300 import prepare, prepare_sage
@@ -309,25 +311,26 @@ def variant_ops(dev, stream, qkv, wq, wk, pos, common, spec, iters: int = 20):
     out8 = tuple(torch.empty(shape, dtype=torch.float8_e4m3fn, device=dev) for _ in range(3))
     sc = torch.empty(3, dtype=torch.float32, device=dev)
     table = torch.tensor([0.02, 0.02, 0.01], dtype=torch.float32, device=dev)
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for name, fn, nbytes in (
             ("sage_f32q_f32k_f16v", lambda: prepare_sage(qkv, wq, wk, pos, kv_scale=0.5, out=(qs, ks, vs),
                                                          stream=stream, **common), 16 * n),
             ("e4m3_static", lambda: prepare(qkv, wq, wk, pos, scale_mode="static", static_scales=table,
                                             out=out8, out_scales=sc, stream=stream, **common), 9 * n)):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize(dev)
         ts = []
-        for _ in range(iters):
+        for i in range(3 + iters):
+            scratch.fill_(i & 0xFF)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
             b.record(stream)
-            torch.cuda.synchronize(dev)
-            ts.append(a.elapsed_time(b))
-        ms = statistics.fmean(ts)
-        rows[name] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9, "bytes": nbytes}
-    del qs, ks, vs, out8
+            b.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        rows[name] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9, "bytes": nbytes,
+                      "l2": "flushed before each call (256 MB write)"}
+    del qs, ks, vs, out8, scratch
     torch.cuda.empty_cache()
     return rows
 

@@ -401,6 +401,32 @@ void h3qk_launch_count_reset(void);
 /* Library version, major*10000 + minor*100 + patch. */
 int h3qk_version(void);
 
+/*
+ * Debug builds.  `python -m video_vae_decoder_qkv_gb300.build --debug` builds
+ * libh3qk_debug.so with device-side bounds checks, in place of a memory
+ * sanitizer.  Every
+ * global load, store and atomic of the QK-prep kernels is checked against
+ * the extent of its buffer first.  A failed check is recorded in status
+ * words on the device and the access is skipped; nothing traps.
+ *
+ * h3qk_debug_checks: 1 in a debug build, 0 in the release library.
+ * h3qk_debug_status: copies the current device's four status words to
+ *   out[4] (synchronous; waits for all work on the device to finish):
+ *   out[0] the OR of the failed checks (1 packed-row load, 2 output store,
+ *   4 position load, 8 per-item length load, 16 amax word / descale /
+ *   counter index), out[1] the number of failures, out[2..3] the first
+ *   failing element offset + 1 as a little-endian 64-bit value (0: none).
+ *   With reset != 0 it then zeroes them.  H3QK_ERR_INVALID_ARG in a release
+ *   build or for a NULL out.
+ * h3qk_debug_limit_outputs: a test hook.  elements >= 0 makes later calls
+ *   of this process treat each output tensor as holding at most `elements`
+ *   elements, so the checks report and skip the stores past it; a negative
+ *   value restores the calls' own extents.  No effect in a release build.
+ */
+int h3qk_debug_checks(void);
+h3qk_status h3qk_debug_status(uint32_t* out, int reset);
+void h3qk_debug_limit_outputs(int64_t elements);
+
 #ifdef __cplusplus
 }
 #endif

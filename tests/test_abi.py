@@ -363,3 +363,24 @@ def test_split_cast_counters_not_over_the_amax():
     o = opts(sat_counts=TAB + 4)
     st = L.h3qk_cast(QKV, WQ, WK, POS, N, H, D, R, N, TAB, OQ, OK_, OV, SC, C.byref(o), None)
     assert st == h3qk.ERR_ALIAS
+
+
+@pytest.mark.pure_host
+def test_release_build_has_no_debug_checks(L):
+    import ctypes as C
+
+    assert L.h3qk_debug_checks() == 0
+    out = (C.c_uint32 * 4)()
+    assert L.h3qk_debug_status(out, 0) == h3qk.ERR_INVALID_ARG
+    L.h3qk_debug_limit_outputs(-1)   # no effect in a release build
+
+
+@pytest.mark.pure_host
+def test_debug_build_compiles_and_reports_itself():
+    """The debug library (kernels with device-side bounds checks) builds for
+    sm_103a and says so; nothing here launches a kernel."""
+    from video_vae_decoder_qkv_gb300 import build as B
+
+    D = h3qk.load_library(B.build(debug=True))
+    assert D.h3qk_debug_checks() == 1
+    assert D.h3qk_version() == h3qk.lib().h3qk_version()

@@ -20,6 +20,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libh3qk.so")
+# The same sources with the kernels' device-side bounds checks compiled in
+# (H3QK_DEBUG_CHECKS=1; include/h3qk.h, "Debug builds").
+LIB_DEBUG = os.path.join(PKG, "libh3qk_debug.so")
 # The kernel instances of each input type sit in their own translation unit
 # so that the sources compile in parallel.
 SOURCES = [os.path.join(CSRC, f) for f in ("h3qk_api.cu", "h3qk_host.cu", "h3qk_launch_bf16.cu",
@@ -46,17 +49,22 @@ def nvcc_path() -> str:
     raise RuntimeError("nvcc not found (set NVCC or put the CUDA toolkit on PATH)")
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in DEPS)
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    if not force and up_to_date():
-        return LIB
-    tag = f".tmp{os.getpid()}"
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None, debug: bool = False) -> str:
+    """Build libh3qk.so (or, with debug, libh3qk_debug.so with the device-side
+    bounds checks) unless it is newer than every source."""
+    out = LIB_DEBUG if debug else LIB
+    if debug:
+        extra = [*(extra or []), "-DH3QK_DEBUG_CHECKS=1"]
+    if not force and up_to_date(out):
+        return out
+    tag = f".tmp{os.getpid()}{'d' if debug else ''}"
     objs = [os.path.join(PKG, os.path.basename(src) + tag + ".o") for src in SOURCES]
 
     def compile_one(src_obj):
@@ -73,16 +81,15 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     try:
         with ThreadPoolExecutor(len(SOURCES)) as ex:
             list(ex.map(compile_one, zip(SOURCES, objs)))
-        tmp = LIB + tag
+        tmp = out + tag
         subprocess.run([nvcc_path(), *LINK_FLAGS, "-o", tmp, *objs], check=True)
-        os.replace(tmp, LIB)
+        os.replace(tmp, out)
     finally:
         for o in objs:
             if os.path.exists(o):
                 os.remove(o)
-    return LIB
+    return out
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

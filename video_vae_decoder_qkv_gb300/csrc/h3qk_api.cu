@@ -64,6 +64,39 @@ h3qk_status fail_cuda(cudaError_t e)
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Debug builds: the status words of the kernels' bounds checks (dbg_ok in
+// h3qk_kernels.cuh), one set per device, and a test hook that narrows the
+// output extent the checks allow.
+// ---------------------------------------------------------------------------
+#if H3QK_DEBUG_CHECKS
+static __device__ __align__(16) unsigned int g_dbg_status[4];
+#endif
+namespace {
+std::mutex g_dbg_mu;
+unsigned int* g_dbg_addr[kMaxDevices] = {nullptr};
+int64_t g_dbg_out_limit = -1;  // < 0: the call's own output extent
+}  // namespace
+
+// Device address of the status words on the current device (null in release
+// builds or when it cannot be looked up; the checks then only skip).
+static unsigned int* dbg_status_addr()
+{
+#if H3QK_DEBUG_CHECKS
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_dbg_mu);
+    if (!g_dbg_addr[dev]) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_dbg_status) != cudaSuccess) return nullptr;
+        g_dbg_addr[dev] = static_cast<unsigned int*>(a);
+    }
+    return g_dbg_addr[dev];
+#else
+    return nullptr;
+#endif
+}
+
 int h3qk_internal_sm_count() { return sm_count(); }
 void h3qk_internal_count_launch() { ++g_launches; }
 h3qk_status h3qk_internal_fail_cuda(cudaError_t e) { return fail_cuda(e); }
@@ -105,7 +138,25 @@ uint64_t h3qk_launch_count(void) { return g_launches; }
 
 void h3qk_launch_count_reset(void) { g_launches = 0; }
 
-int h3qk_version(void) { return 100; }
+int h3qk_version(void) { return 101; }
+
+int h3qk_debug_checks(void) { return H3QK_DEBUG_CHECKS ? 1 : 0; }
+
+h3qk_status h3qk_debug_status(uint32_t* out, int reset)
+{
+    if (!out || !H3QK_DEBUG_CHECKS) return H3QK_ERR_INVALID_ARG;
+    unsigned int* a = dbg_status_addr();
+    if (!a) return h3qk_internal_fail_cuda(cudaErrorInvalidSymbol);
+    cudaError_t e = cudaMemcpy(out, a, 16, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && reset) e = cudaMemset(a, 0, 16);
+    return e == cudaSuccess ? H3QK_OK : h3qk_internal_fail_cuda(e);
+}
+
+void h3qk_debug_limit_outputs(int64_t elements)
+{
+    std::lock_guard<std::mutex> lock(g_dbg_mu);
+    g_dbg_out_limit = elements;
+}
 
 }  // extern "C"
 
@@ -216,6 +267,12 @@ h3qk_status plan_inputs(const void* qkv, const float* norm_wq, const float* norm
     p.in_part_off[1] = HD;
     p.in_part_off[2] = 2 * HD;
     p.pf_span = parts * HD;
+    p.dbg_status = dbg_status_addr();
+    p.dbg_out_elems = tokens * HD;
+    {
+        std::lock_guard<std::mutex> lock(g_dbg_mu);
+        if (g_dbg_out_limit >= 0 && g_dbg_out_limit < p.dbg_out_elems) p.dbg_out_elems = g_dbg_out_limit;
+    }
     p.qk_first = 0;
     p.qk_end = 2;
     p.has_v = 1;

@@ -214,6 +214,8 @@ struct Params {
                                  // call's previous kernel (see the griddepcontrol notes)
     int32_t reverse;             // walk the row groups from the last one down (the cast
                                  // after an amax pass: see the note in the kernel)
+    unsigned int* dbg_status;    // debug builds: the check status words (see dbg_ok); else null
+    int64_t dbg_out_elems;       // debug builds: elements of each output tensor the checks allow
     float2 one2;                 // {1, 1} and {-1, -1}: the unit factors of the packed sums
     float2 mone2;                // (see fma2 below); read at run time, never constants
     int64_t pf_span;             // elements of an input row the call reads ([0, pf_span))
@@ -222,6 +224,52 @@ struct Params {
     float inv_freq[kMaxPairs];   // per rotary pair
     uint8_t axis[kMaxPairs];     // position axis of each rotary pair
 };
+
+// ---------------------------------------------------------------------------
+// Debug builds (H3QK_DEBUG_CHECKS=1): every global access of qkprep_kernel is
+// checked against the extent of its buffer before it is made.  A failed check
+// ORs its bit into status word 0, counts itself in word 1, keeps the first
+// offending offset + 1 in words 2-3 (64-bit), and the access is skipped, so
+// a wrong index is reported and never made.  Release builds compile every
+// check to `true`.
+// ---------------------------------------------------------------------------
+#ifndef H3QK_DEBUG_CHECKS
+#define H3QK_DEBUG_CHECKS 0
+#endif
+enum DbgCheck : unsigned int {
+    kDbgInput = 1u,      // a 16-byte load of the packed rows
+    kDbgOutput = 2u,     // a store of 8 output elements
+    kDbgPositions = 4u,  // a position load
+    kDbgLengths = 8u,    // a per-item valid length load
+    kDbgSlot = 16u       // an amax word, descale or counter index
+};
+__device__ __forceinline__ bool dbg_ok(const Params& p, bool ok, unsigned int what, int64_t at)
+{
+    if constexpr (H3QK_DEBUG_CHECKS) {
+        if (!ok && p.dbg_status) {
+            atomicOr(p.dbg_status, what);
+            atomicAdd(p.dbg_status + 1, 1u);
+            atomicCAS(reinterpret_cast<unsigned long long*>(p.dbg_status + 2), 0ull,
+                      static_cast<unsigned long long>(at) + 1ull);
+        }
+        return ok;
+    } else {
+        return true;
+    }
+}
+// The checks of one access kind, by offset in elements of the buffer.
+__device__ __forceinline__ bool dbg_in(const Params& p, int64_t at)
+{
+    return dbg_ok(p, at >= 0 && at + 8 <= (p.rows - 1) * p.row_stride + p.pf_span, kDbgInput, at);
+}
+__device__ __forceinline__ bool dbg_out(const Params& p, int64_t at)
+{
+    return dbg_ok(p, at >= 0 && at + 8 <= p.dbg_out_elems, kDbgOutput, at);
+}
+__device__ __forceinline__ bool dbg_slot(const Params& p, int slot)
+{
+    return dbg_ok(p, slot >= 0 && slot < 3, kDbgSlot, slot);
+}
 
 // ---------------------------------------------------------------------------
 // Sine and cosine of a binary32 angle: the library's own routine (Cody & Waite
@@ -989,7 +1037,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
         if (rr < p.rows) {
             const int64_t bb = rr / p.seq;
             int64_t vl = p.valid_len;
-            if (p.valid_lens) {
+            if (p.valid_lens && dbg_ok(p, bb < p.rows / p.seq, kDbgLengths, bb)) {
                 vl = __ldg(p.valid_lens + bb);
                 vl = vl < 0 ? 0 : (vl > p.seq ? p.seq : vl);
             }
@@ -1007,9 +1055,11 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                 for (int u = 0; u < U; ++u)
 #pragma unroll
                     for (int q = 0; q < CH; ++q)
-                        if (fh0 + u < fh_hi && fact[q])
-                            cp_async16(st + (u * CH + q) * 32 + lane,
-                                       frow + p.in_part_off[fpart] + static_cast<int64_t>(fh0 + u) * D + 8 * q * LPR);
+                        if (fh0 + u < fh_hi && fact[q]) {
+                            const uint16_t* src_u =
+                                frow + p.in_part_off[fpart] + static_cast<int64_t>(fh0 + u) * D + 8 * q * LPR;
+                            if (dbg_in(p, src_u - p.qkv)) cp_async16(st + (u * CH + q) * 32 + lane, src_u);
+                        }
                 fh0 += U;
                 if (fh0 >= fh_hi) {
                     fh0 = fh_lo;
@@ -1047,7 +1097,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
         for (int t = 0; t < 3; ++t) {
             if (p.slot[t] < 0) continue;
             // One load from whichever table this mode uses (never a NULL pointer).
-            const float a = __uint_as_float(__ldcg(p.scale_words + p.slot[t]));
+            const float a = dbg_slot(p, p.slot[t]) ? __uint_as_float(__ldcg(p.scale_words + p.slot[t])) : 0.0f;
             const bool ok = a >= 1.17549435e-38f && a <= 3.40282347e+38f;
             float s = 1.0f, f = 1.0f;
             if (ok) {
@@ -1060,7 +1110,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                 }
             }
             fac[t] = f;
-            if (blockIdx.x == 0 && threadIdx.x == 0) p.out_scales[p.slot[t]] = s;
+            if (blockIdx.x == 0 && threadIdx.x == 0 && dbg_slot(p, p.slot[t])) p.out_scales[p.slot[t]] = s;
         }
     }
 
@@ -1075,7 +1125,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
             b = r / p.seq;
             s = r - b * p.seq;
             int64_t vl = p.valid_len;
-            if (p.valid_lens) {
+            if (p.valid_lens && dbg_ok(p, b < p.rows / p.seq, kDbgLengths, b)) {
                 vl = __ldg(p.valid_lens + b);
                 vl = vl < 0 ? 0 : (vl > p.seq ? p.seq : vl);
             }
@@ -1105,7 +1155,10 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                 for (int i = 0; i < 4; ++i) {
                     const int pair = 4 * (c + q * LPR) + i;
                     if (rot[q][i] && act[q]) {
-                        const float pv = static_cast<float>(__ldg(p.pos + r * p.n_axes + p.axis[pair]));
+                        const int64_t pi = r * p.n_axes + p.axis[pair];
+                        const float pv = dbg_ok(p, pi >= 0 && pi < p.rows * p.n_axes, kDbgPositions, pi)
+                                             ? static_cast<float>(__ldg(p.pos + pi))
+                                             : 0.0f;
                         sincos_h3(__fmul_rn(pv, p.inv_freq[pair]), sn[q][i], cs[q][i]);
                     }
                 }
@@ -1145,7 +1198,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                     // Once per part: re-reading every batch made the three amax
                     // words a hot spot for every warp of the grid.
                     if (h0 == h_lo) {
-                        const uint32_t gw = lane == 0 ? __ldcg(p.amax_words + p.slot[part]) : 0u;
+                        const uint32_t gw =
+                            lane == 0 && dbg_slot(p, p.slot[part]) ? __ldcg(p.amax_words + p.slot[part]) : 0u;
                         thr[part] = __shfl_sync(0xffffffffu, gw, 0);
                     }
                 }
@@ -1171,8 +1225,10 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
 #pragma unroll
                         for (int q = 0; q < CH; ++q) {
                             raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
-                            if (h0 + u < h_hi && act[q])
-                                raw[u][q] = load16(src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR);
+                            if (h0 + u < h_hi && act[q]) {
+                                const uint16_t* a = src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR;
+                                if (dbg_in(p, a - p.qkv)) raw[u][q] = load16(a);
+                            }
                         }
                 }
 #pragma unroll
@@ -1220,7 +1276,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                         for (int q = 0; q < CH; ++q) {
                             if (!act[q]) continue;
                             const int64_t off = obase + h * p.out_hstride + 8 * q * LPR;
-                            store_f32x8(yf[q], p.kv_scale, part == 1, static_cast<float*>(p.out[part]) + off);
+                            if (dbg_out(p, off))
+                                store_f32x8(yf[q], p.kv_scale, part == 1, static_cast<float*>(p.out[part]) + off);
                         }
                         continue;
                     }
@@ -1238,7 +1295,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                             p.eps, D, p.one2, p.mone2, act, amf[part]);
                         run[part] = __reduce_max_sync(0xffffffffu, __float_as_uint(amf[part]));
                         if (run[part] > pub[part]) {  // warp-uniform
-                            if (lane == 0) atomicMax(p.amax_words + p.slot[part], run[part]);
+                            if (lane == 0 && dbg_slot(p, p.slot[part])) atomicMax(p.amax_words + p.slot[part], run[part]);
                             pub[part] = run[part];
                         }
                         continue;
@@ -1259,7 +1316,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                         for (int q = 0; q < CH; ++q) {
                             if (!act[q]) continue;
                             const int64_t off = obase + h * p.out_hstride + 8 * q * LPR;
-                            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out[part]) + off) = code[q];
+                            if (dbg_out(p, off))
+                                *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out[part]) + off) = code[q];
                         }
                         continue;
                     }
@@ -1272,19 +1330,20 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                         const int64_t off = obase + h * p.out_hstride + 8 * q * LPR;
                         if constexpr (MODE == kOut16) {
                             uint16_t* dst = static_cast<uint16_t*>(p.out[part]) + off;
-                            *reinterpret_cast<uint4*>(dst) = make_uint4(y[q][0], y[q][1], y[q][2], y[q][3]);
+                            if (dbg_out(p, off))
+                                *reinterpret_cast<uint4*>(dst) = make_uint4(y[q][0], y[q][1], y[q][2], y[q][3]);
                         } else if constexpr (MODE == kAmax) {
 #pragma unroll
                             for (int i = 0; i < 4; ++i) am[part] = hmax2x<BF16>(am[part], y[q][i]);
                         } else {
                             uint8_t* dst = static_cast<uint8_t*>(p.out[part]) + off;
-                            emit_e4m3<BF16, count_sat>(y[q], fac[part], dst, sat[part]);
+                            if (dbg_out(p, off)) emit_e4m3<BF16, count_sat>(y[q], fac[part], dst, sat[part]);
                         }
                     }
                     if constexpr (MODE == kAmax) {
                         run[part] = __reduce_max_sync(0xffffffffu, __float_as_uint(hmax2x_to_float<BF16>(am[part])));
                         if (run[part] > pub[part]) {  // warp-uniform
-                            if (lane == 0) atomicMax(p.amax_words + p.slot[part], run[part]);
+                            if (lane == 0 && dbg_slot(p, p.slot[part])) atomicMax(p.amax_words + p.slot[part], run[part]);
                             pub[part] = run[part];
                         }
                     }
@@ -1314,8 +1373,10 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
 #pragma unroll
                         for (int q = 0; q < CH; ++q) {
                             raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
-                            if (h0 + u < h_hi && act[q])
-                                raw[u][q] = load16(src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR);
+                            if (h0 + u < h_hi && act[q]) {
+                                const uint16_t* a = src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR;
+                                if (dbg_in(p, a - p.qkv)) raw[u][q] = load16(a);
+                            }
                         }
                 }
 #pragma unroll
@@ -1328,16 +1389,17 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                         const int64_t off = obase + h * p.out_hstride + 8 * q * LPR;
                         if constexpr (MODE == kOut16) {
                             uint16_t* dst = static_cast<uint16_t*>(p.out[2]) + off;
-                            *reinterpret_cast<uint4*>(dst) = raw[u][q];
+                            if (dbg_out(p, off)) *reinterpret_cast<uint4*>(dst) = raw[u][q];
                         } else if constexpr (MODE == kSage) {
-                            store_v_f16<BF16>(raw[u][q], p.kv_scale, static_cast<uint16_t*>(p.out[2]) + off);
+                            if (dbg_out(p, off))
+                                store_v_f16<BF16>(raw[u][q], p.kv_scale, static_cast<uint16_t*>(p.out[2]) + off);
                         } else if constexpr (MODE == kAmax) {
 #pragma unroll
                             for (int i = 0; i < 4; ++i) am[2] = hmax2x<BF16>(am[2], word(raw[u][q], i));
                         } else {
                             const uint32_t yv[4] = {raw[u][q].x, raw[u][q].y, raw[u][q].z, raw[u][q].w};
                             uint8_t* dst = static_cast<uint8_t*>(p.out[2]) + off;
-                            emit_e4m3<BF16, count_sat>(yv, fac[2], dst, sat[2]);
+                            if (dbg_out(p, off)) emit_e4m3<BF16, count_sat>(yv, fac[2], dst, sat[2]);
                         }
                     }
                 }
@@ -1363,7 +1425,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
 #pragma unroll
             for (int w = 0; w < Shape<MODE, LPR>::W; ++w) m = fmaxf(m, red[threadIdx.x][w]);
             // Non-negative binary32 values order like their bit patterns.
-            if (m > 0.0f) atomicMax(p.amax_words + p.slot[threadIdx.x], __float_as_uint(m));
+            if (m > 0.0f && dbg_slot(p, p.slot[threadIdx.x]))
+                atomicMax(p.amax_words + p.slot[threadIdx.x], __float_as_uint(m));
         }
     }
     if constexpr (count_sat) {
@@ -1372,7 +1435,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
             unsigned int n = sat[t];
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-            if (lane == 0 && n > 0 && p.slot[t] >= 0) atomicAdd(p.sat_counts + p.slot[t], n);
+            if (lane == 0 && n > 0 && p.slot[t] >= 0 && dbg_slot(p, p.slot[t])) atomicAdd(p.sat_counts + p.slot[t], n);
         }
     }
 }

@@ -56,29 +56,40 @@ class Opts(ctypes.Structure):
 _lib = None
 
 
+def load_library(path: str) -> ctypes.CDLL:
+    """Load a build of the library at `path` with the C signatures set (the
+    release libh3qk.so through lib(), or the debug build libh3qk_debug.so)."""
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m video_vae_decoder_qkv_gb300.build` "
+            "(or __graft_entry__.build()); there is no other implementation of this path")
+    L = ctypes.CDLL(path)
+    P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    L.h3qk_prepare.restype = ctypes.c_int
+    L.h3qk_prepare.argtypes = [P, P, P, P, I64, I32, I32, I32, I64, ctypes.c_int, ctypes.c_int,
+                               P, P, P, P, ctypes.POINTER(Opts), P]
+    L.h3qk_opts_init.restype = None
+    L.h3qk_opts_init.argtypes = [ctypes.POINTER(Opts)]
+    L.h3qk_workspace_bytes.restype = ctypes.c_size_t
+    L.h3qk_status_string.restype = ctypes.c_char_p
+    L.h3qk_status_string.argtypes = [ctypes.c_int]
+    L.h3qk_last_cuda_error.restype = ctypes.c_int
+    L.h3qk_launch_count.restype = ctypes.c_uint64
+    L.h3qk_launch_count_reset.restype = None
+    L.h3qk_version.restype = ctypes.c_int
+    L.h3qk_debug_checks.restype = ctypes.c_int
+    L.h3qk_debug_status.restype = ctypes.c_int
+    L.h3qk_debug_status.argtypes = [P, ctypes.c_int]
+    L.h3qk_debug_limit_outputs.restype = None
+    L.h3qk_debug_limit_outputs.argtypes = [I64]
+    return L
+
+
 def lib() -> ctypes.CDLL:
     """Load libh3qk.so; raise if it was not built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(
-                f"{LIB_PATH} is missing: build it with `python -m video_vae_decoder_qkv_gb300.build` "
-                "(or __graft_entry__.build()); there is no other implementation of this path")
-        L = ctypes.CDLL(LIB_PATH)
-        P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-        L.h3qk_prepare.restype = ctypes.c_int
-        L.h3qk_prepare.argtypes = [P, P, P, P, I64, I32, I32, I32, I64, ctypes.c_int, ctypes.c_int,
-                                   P, P, P, P, ctypes.POINTER(Opts), P]
-        L.h3qk_opts_init.restype = None
-        L.h3qk_opts_init.argtypes = [ctypes.POINTER(Opts)]
-        L.h3qk_workspace_bytes.restype = ctypes.c_size_t
-        L.h3qk_status_string.restype = ctypes.c_char_p
-        L.h3qk_status_string.argtypes = [ctypes.c_int]
-        L.h3qk_last_cuda_error.restype = ctypes.c_int
-        L.h3qk_launch_count.restype = ctypes.c_uint64
-        L.h3qk_launch_count_reset.restype = None
-        L.h3qk_version.restype = ctypes.c_int
-        _lib = L
+        _lib = load_library(LIB_PATH)
     return _lib
 
 
