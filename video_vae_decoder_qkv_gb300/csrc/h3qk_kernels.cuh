@@ -76,6 +76,11 @@ constexpr int kWarpsPerBlock = 8;    // head_dim > 64; see Shape for head_dim <=
 #define H3QK_ROT_FIRST_MIN_LPR 8
 #endif
 
+// 1: the amax pass walks each work item backwards (see kBack in the kernel).
+#ifndef H3QK_AMAX_BACK
+#define H3QK_AMAX_BACK 1
+#endif
+
 // The amax pass's pairwise second bound (qk_pair_may_exceed) runs in the
 // instances whose warps hold at least this many token rows.
 #ifndef H3QK_AMAX_PAIR_MIN_TPW
@@ -959,6 +964,12 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
         const int64_t g0 = item >> hs_shift;
         return rev ? n_groups - 1 - g0 : g0;
     };
+    // The amax pass walks each work item backwards: V, then K, then Q, each
+    // from its last batch of heads down.  What it reads last in an item is
+    // then what the cast (reversed groups, forward within an item) reads
+    // first, so the cast's first reads hit the lines the amax pass left in
+    // L2.  The maximum does not depend on the order.
+    constexpr bool kBack = MODE == kAmax && H3QK_AMAX_BACK;
     constexpr int NT = Shape<MODE, LPR>::NT;  // threads per block
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * NT + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * NT) >> 5;
@@ -1018,10 +1029,12 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     // Each lane copies its own 16-byte chunks of the batch S-1 steps ahead
     // into its warp's ring of S stages, walking the same sequence of batches
     // the loop below consumes (groups, then parts Q, K, V, then head
-    // batches); stage layout [S][U][CH][32 lanes] of uint4.
+    // batches; kBack: parts V, K, Q and head batches from the last one
+    // down); stage layout [S][U][CH][32 lanes] of uint4.
     extern __shared__ __align__(16) uint4 h3qk_stage[];
     uint4* const ring = h3qk_stage + static_cast<size_t>(threadIdx.x >> 5) * (S > 0 ? S * U * CH * 32 : 0);
-    const int first_part = p.qk_first < p.qk_end ? p.qk_first : 2;
+    const bool has_qk = p.qk_first < p.qk_end;
+    const int first_part = kBack ? (p.has_v || !has_qk ? 2 : p.qk_end - 1) : (has_qk ? p.qk_first : 2);
     int64_t fit = warp0;         // issue cursor: work item, part, head, stage
     int fpart = first_part, fh0 = 0, fh_lo = 0, fh_hi = H, fstage = 0;
     const uint16_t* frow = p.qkv;
@@ -1030,8 +1043,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
         if constexpr (SLICED) {
             fh_lo = static_cast<int>(fit & hs_mask) * p.hs_heads;
             fh_hi = min(H, fh_lo + p.hs_heads);
-            fh0 = fh_lo;
         }
+        fh0 = kBack ? fh_lo + (fh_hi - fh_lo - 1) / U * U : fh_lo;
         const int64_t rr = group_of(fit) * TPW + sub;
         bool ok = false;
         if (rr < p.rows) {
@@ -1060,17 +1073,33 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                                 frow + p.in_part_off[fpart] + static_cast<int64_t>(fh0 + u) * D + 8 * q * LPR;
                             if (dbg_in(p, src_u - p.qkv)) cp_async16(st + (u * CH + q) * 32 + lane, src_u);
                         }
-                fh0 += U;
-                if (fh0 >= fh_hi) {
-                    fh0 = fh_lo;
-                    if (fpart < 2 && fpart + 1 < p.qk_end) {
-                        ++fpart;
-                    } else if (fpart < 2 && p.has_v) {
-                        fpart = 2;
-                    } else {
-                        fpart = first_part;
-                        fit += n_warps;
-                        if (fit < n_items) feed_group();
+                if constexpr (kBack) {
+                    fh0 -= U;
+                    if (fh0 < fh_lo) {
+                        fh0 = fh_lo + (fh_hi - fh_lo - 1) / U * U;
+                        if (fpart == 2 && has_qk) {
+                            fpart = p.qk_end - 1;
+                        } else if (fpart < 2 && fpart > p.qk_first) {
+                            --fpart;
+                        } else {
+                            fpart = first_part;
+                            fit += n_warps;
+                            if (fit < n_items) feed_group();
+                        }
+                    }
+                } else {
+                    fh0 += U;
+                    if (fh0 >= fh_hi) {
+                        fh0 = fh_lo;
+                        if (fpart < 2 && fpart + 1 < p.qk_end) {
+                            ++fpart;
+                        } else if (fpart < 2 && p.has_v) {
+                            fpart = 2;
+                        } else {
+                            fpart = first_part;
+                            fit += n_warps;
+                            if (fit < n_items) feed_group();
+                        }
                     }
                 }
             }
@@ -1187,17 +1216,78 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
             }
         };
 
-        // ---- Q and K: norm + RoPE ------------------------------------------
+        // ---- V: passed through ----------------------------------------------
+        auto v_part = [&]() {
+            const uint16_t* src = rowp + p.in_part_off[2];
+            const int hv_first = kBack ? h_lo + (h_hi - h_lo - 1) / UV * UV : h_lo;  // first batch of heads
+            for (int h0 = hv_first; kBack ? h0 >= h_lo : h0 < h_hi; h0 += kBack ? -UV : UV) {
+                prefetch(p.in_part_off[2] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(UV) * D);
+                uint4 raw[UV][CH];
+                if constexpr (S > 0) {
+                    issue();
+                    cp_async_wait<(S > 0 ? S - 1 : 0)>();
+                    const uint4* st = ring + pstage * (U * CH * 32);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
+                    for (int u = 0; u < UV; ++u)
+#pragma unroll
+                        for (int q = 0; q < CH; ++q)
+                            raw[u][q] = on[q] ? st[(u * CH + q) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                    pstage = pstage + 1 == S ? 0 : pstage + 1;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < UV; ++u)
+#pragma unroll
+                        for (int q = 0; q < CH; ++q) {
+                            raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
+                            if (h0 + u < h_hi && act[q]) {
+                                const uint16_t* a = src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR;
+                                if (dbg_in(p, a - p.qkv)) raw[u][q] = load16(a);
+                            }
+                        }
+                }
+#pragma unroll
+                for (int u = 0; u < UV; ++u) {
+                    const int h = h0 + u;
+                    if (h >= h_hi) break;  // warp-uniform
+#pragma unroll
+                    for (int q = 0; q < CH; ++q) {
+                        if (!act[q]) continue;
+                        const int64_t off = obase + h * p.out_hstride + 8 * q * LPR;
+                        if constexpr (MODE == kOut16) {
+                            uint16_t* dst = static_cast<uint16_t*>(p.out[2]) + off;
+                            if (dbg_out(p, off)) *reinterpret_cast<uint4*>(dst) = raw[u][q];
+                        } else if constexpr (MODE == kSage) {
+                            if (dbg_out(p, off))
+                                store_v_f16<BF16>(raw[u][q], p.kv_scale, static_cast<uint16_t*>(p.out[2]) + off);
+                        } else if constexpr (MODE == kAmax) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) am[2] = hmax2x<BF16>(am[2], word(raw[u][q], i));
+                        } else {
+                            const uint32_t yv[4] = {raw[u][q].x, raw[u][q].y, raw[u][q].z, raw[u][q].w};
+                            uint8_t* dst = static_cast<uint8_t*>(p.out[2]) + off;
+                            if (dbg_out(p, off)) emit_e4m3<BF16, count_sat>(yv, fac[2], dst, sat[2]);
+                        }
+                    }
+                }
+            }
+        };
+
+        // ---- Q and K: norm + RoPE ------------------------------------------
+        if constexpr (kBack) {
+            if (p.has_v) v_part();
+        }
+#pragma unroll
+        for (int pi = 0; pi < 2; ++pi) {
+            const int part = kBack ? 1 - pi : pi;
             if (part < p.qk_first || part >= p.qk_end) continue;  // warp-uniform
             const uint16_t* src = rowp + p.in_part_off[part];
-            for (int h0 = h_lo; h0 < h_hi; h0 += U) {
+            const int h_first = kBack ? h_lo + (h_hi - h_lo - 1) / U * U : h_lo;  // first batch of heads
+            for (int h0 = h_first; kBack ? h0 >= h_lo : h0 < h_hi; h0 += kBack ? -U : U) {
                 prefetch(p.in_part_off[part] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(U) * D);
                 if constexpr (MODE == kAmax) {
                     // Once per part: re-reading every batch made the three amax
                     // words a hot spot for every warp of the grid.
-                    if (h0 == h_lo) {
+                    if (h0 == h_first) {
                         const uint32_t gw =
                             lane == 0 && dbg_slot(p, p.slot[part]) ? __ldcg(p.amax_words + p.slot[part]) : 0u;
                         thr[part] = __shfl_sync(0xffffffffu, gw, 0);
@@ -1350,60 +1440,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                 }
             }
         }
-
-        // ---- V: passed through ----------------------------------------------
-        if (p.has_v) {
-            const uint16_t* src = rowp + p.in_part_off[2];
-            for (int h0 = h_lo; h0 < h_hi; h0 += UV) {
-                prefetch(p.in_part_off[2] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(UV) * D);
-                uint4 raw[UV][CH];
-                if constexpr (S > 0) {
-                    issue();
-                    cp_async_wait<(S > 0 ? S - 1 : 0)>();
-                    const uint4* st = ring + pstage * (U * CH * 32);
-#pragma unroll
-                    for (int u = 0; u < UV; ++u)
-#pragma unroll
-                        for (int q = 0; q < CH; ++q)
-                            raw[u][q] = on[q] ? st[(u * CH + q) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
-                    pstage = pstage + 1 == S ? 0 : pstage + 1;
-                } else {
-#pragma unroll
-                    for (int u = 0; u < UV; ++u)
-#pragma unroll
-                        for (int q = 0; q < CH; ++q) {
-                            raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
-                            if (h0 + u < h_hi && act[q]) {
-                                const uint16_t* a = src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR;
-                                if (dbg_in(p, a - p.qkv)) raw[u][q] = load16(a);
-                            }
-                        }
-                }
-#pragma unroll
-                for (int u = 0; u < UV; ++u) {
-                    const int h = h0 + u;
-                    if (h >= h_hi) break;  // warp-uniform
-#pragma unroll
-                    for (int q = 0; q < CH; ++q) {
-                        if (!act[q]) continue;
-                        const int64_t off = obase + h * p.out_hstride + 8 * q * LPR;
-                        if constexpr (MODE == kOut16) {
-                            uint16_t* dst = static_cast<uint16_t*>(p.out[2]) + off;
-                            if (dbg_out(p, off)) *reinterpret_cast<uint4*>(dst) = raw[u][q];
-                        } else if constexpr (MODE == kSage) {
-                            if (dbg_out(p, off))
-                                store_v_f16<BF16>(raw[u][q], p.kv_scale, static_cast<uint16_t*>(p.out[2]) + off);
-                        } else if constexpr (MODE == kAmax) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) am[2] = hmax2x<BF16>(am[2], word(raw[u][q], i));
-                        } else {
-                            const uint32_t yv[4] = {raw[u][q].x, raw[u][q].y, raw[u][q].z, raw[u][q].w};
-                            uint8_t* dst = static_cast<uint8_t*>(p.out[2]) + off;
-                            if (dbg_out(p, off)) emit_e4m3<BF16, count_sat>(yv, fac[2], dst, sat[2]);
-                        }
-                    }
-                }
-            }
+        if constexpr (!kBack) {
+            if (p.has_v) v_part();
         }
     }
 
