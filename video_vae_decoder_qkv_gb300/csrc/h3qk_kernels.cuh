@@ -76,6 +76,12 @@ constexpr int kWarpsPerBlock = 8;    // head_dim > 64; see Shape for head_dim <=
 #define H3QK_ROT_FIRST_MIN_LPR 8
 #endif
 
+// 1: the kRotFirst cast instances keep the rotary cos/sin of a row group in
+// shared memory instead of registers (see kAngSmem in the kernel).
+#ifndef H3QK_SMEM_ANGLES
+#define H3QK_SMEM_ANGLES 1
+#endif
+
 // 1: the amax pass walks each work item backwards (see kBack in the kernel).
 #ifndef H3QK_AMAX_BACK
 #define H3QK_AMAX_BACK 1
@@ -922,6 +928,15 @@ __device__ __forceinline__ void emit_e4m3(const uint32_t (&y)[4], float f, uint8
 // kCastCount does the same and adds the clipped-value counts; kSage writes
 // binary32 Q, binary32 K * kv_scale and binary16 V * kv_scale.
 // ---------------------------------------------------------------------------
+// Item (batch index) of token row r < p.rows: r / seq, without a division
+// when the call has one item, and in 32 bits when the rows fit.
+__device__ __forceinline__ int64_t item_of(const Params& p, int64_t r)
+{
+    if (p.rows == p.seq) return 0;
+    if (p.rows <= 0x7fffffff) return static_cast<int64_t>(static_cast<uint32_t>(r) / static_cast<uint32_t>(p.seq));
+    return r / p.seq;
+}
+
 template <bool BF16, int LPR, int CH, int MODE, bool SLICED, int RM>
 __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     qkprep_kernel(const __grid_constant__ Params p)
@@ -970,6 +985,15 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     // first, so the cast's first reads hit the lines the amax pass left in
     // L2.  The maximum does not depend on the order.
     constexpr bool kBack = MODE == kAmax && H3QK_AMAX_BACK;
+    // The kRotFirst cast instances (the ones closest to their register cap:
+    // each value of a second chunk keeps its unrotated form until the choice)
+    // keep a row group's rotary cos/sin in shared memory, per warp
+    // [pair slot i][lane] as {cos chunk 0, cos chunk 1, sin chunk 0, sin
+    // chunk 1}: four 16-byte loads per head row instead of 16 registers held
+    // across the group, which halves their spills.
+    constexpr bool kAngSmem = kCastMode && kPairs && CH == 2 && RM == kRotFirst && H3QK_SMEM_ANGLES;
+    __shared__ __align__(16) float4 ang_store[kAngSmem ? Shape<MODE, LPR>::W * 4 * 32 : 1];
+    float4* const angs = ang_store + (kAngSmem ? (threadIdx.x >> 5) * 4 * 32 : 0);
     constexpr int NT = Shape<MODE, LPR>::NT;  // threads per block
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * NT + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * NT) >> 5;
@@ -1048,7 +1072,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
         const int64_t rr = group_of(fit) * TPW + sub;
         bool ok = false;
         if (rr < p.rows) {
-            const int64_t bb = rr / p.seq;
+            const int64_t bb = item_of(p, rr);
             int64_t vl = p.valid_len;
             if (p.valid_lens && dbg_ok(p, bb < p.rows / p.seq, kDbgLengths, bb)) {
                 vl = __ldg(p.valid_lens + bb);
@@ -1109,6 +1133,13 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     };
     int pstage = 0;              // stage of the batch the loop consumes next
     if constexpr (S > 0) {
+        // Chunks past the head are never copied: their slots are zeroed once
+        // here and stay zero, which pads the reduction (each lane owns its
+        // slots, so no other lane writes them).
+#pragma unroll
+        for (int q = 0; q < CH; ++q)
+            if (!on[q])
+                for (int k = 0; k < S * U; ++k) ring[(k * CH + q) * 32 + lane] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int q = 0; q < CH; ++q) fact[q] = false;
         if (fit < n_items) feed_group();
@@ -1151,7 +1182,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
         int64_t b = 0, s = 0;
         bool act_row = false;
         if (r < p.rows) {
-            b = r / p.seq;
+            b = item_of(p, r);
             s = r - b * p.seq;
             int64_t vl = p.valid_len;
             if (p.valid_lens && dbg_ok(p, b < p.rows / p.seq, kDbgLengths, b)) {
@@ -1191,6 +1222,30 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                         sincos_h3(__fmul_rn(pv, p.inv_freq[pair]), sn[q][i], cs[q][i]);
                     }
                 }
+            if constexpr (kAngSmem) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) angs[i * 32 + lane] = make_float4(cs[0][i], cs[1][i], sn[0][i], sn[1][i]);
+            }
+        };
+        // The packed cos / sin of pair slot i for the pair code: from shared
+        // memory (kAngSmem) or from the registers above.
+        auto pair_angles = [&](float2 (&cs2)[CH / 2][4], float2 (&sn2)[CH / 2][4]) {
+            if constexpr (kAngSmem) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 a = angs[i * 32 + lane];
+                    cs2[0][i] = make_float2(a.x, a.y);
+                    sn2[0][i] = make_float2(a.z, a.w);
+                }
+            } else {
+#pragma unroll
+                for (int pp = 0; pp < CH / 2; ++pp)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        cs2[pp][i] = make_float2(cs[2 * pp][i], cs[2 * pp + 1][i]);
+                        sn2[pp][i] = make_float2(sn[2 * pp][i], sn[2 * pp + 1][i]);
+                    }
+            }
         };
         bool have_angles = MODE != kAmax;
         if constexpr (MODE != kAmax) angles();
@@ -1231,7 +1286,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                     for (int u = 0; u < UV; ++u)
 #pragma unroll
                         for (int q = 0; q < CH; ++q)
-                            raw[u][q] = on[q] ? st[(u * CH + q) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                            raw[u][q] = st[(u * CH + q) * 32 + lane];
                     pstage = pstage + 1 == S ? 0 : pstage + 1;
                 } else {
 #pragma unroll
@@ -1296,7 +1351,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                 uint4 raw[U][CH];
                 if constexpr (S > 0) {
                     // Keep the ring S-1 batches ahead, then take this batch.  Only
-                    // chunks past the head are zeroed (they pad the reduction); a
+                    // chunks past the head read as zero (their slots, zeroed at the
+                    // start, pad the reduction); a
                     // padded row's or a missing head's slot holds stale bytes, which
                     // never reach a store, the amax or a count (every use is masked
                     // by act / the head loop, and the amax bound of such a row is 0).
@@ -1307,7 +1363,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                     for (int u = 0; u < U; ++u)
 #pragma unroll
                         for (int q = 0; q < CH; ++q)
-                            raw[u][q] = on[q] ? st[(u * CH + q) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                            raw[u][q] = st[(u * CH + q) * 32 + lane];
                     pstage = pstage + 1 == S ? 0 : pstage + 1;
                 } else {
 #pragma unroll
@@ -1373,13 +1429,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                     }
                     if constexpr (kPairs && MODE == kAmax) {
                         float2 cs2[CH / 2][4], sn2[CH / 2][4];
-#pragma unroll
-                        for (int pp = 0; pp < CH / 2; ++pp)
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                cs2[pp][i] = make_float2(cs[2 * pp][i], cs[2 * pp + 1][i]);
-                                sn2[pp][i] = make_float2(sn[2 * pp][i], sn[2 * pp + 1][i]);
-                            }
+                        pair_angles(cs2, sn2);
                         amf[part] = qk_row_pairs_amax<BF16, LPR, CH, RM>(
                             rw, reinterpret_cast<const float2*>(&ws[part][c][0]), cs2, sn2, rot, rot1, p.inv_d,
                             p.eps, D, p.one2, p.mone2, act, amf[part]);
@@ -1391,13 +1441,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                         continue;
                     } else if constexpr (kPairs) {
                         float2 cs2[CH / 2][4], sn2[CH / 2][4];
-#pragma unroll
-                        for (int pp = 0; pp < CH / 2; ++pp)
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                cs2[pp][i] = make_float2(cs[2 * pp][i], cs[2 * pp + 1][i]);
-                                sn2[pp][i] = make_float2(sn[2 * pp][i], sn[2 * pp + 1][i]);
-                            }
+                        pair_angles(cs2, sn2);
                         uint2 code[CH];
                         qk_row_pairs_e4m3<BF16, LPR, CH, count_sat, RM>(
                             rw, reinterpret_cast<const float2*>(&ws[part][c][0]), cs2, sn2, rot, rot1, p.inv_d,
