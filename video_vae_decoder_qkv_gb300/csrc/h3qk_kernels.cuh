@@ -82,6 +82,13 @@ constexpr int kWarpsPerBlock = 8;    // head_dim > 64; see Shape for head_dim <=
 #define H3QK_SMEM_ANGLES 1
 #endif
 
+// Head split of the amax pass: its warps take 32/LPR/H head rows of H
+// interleaved head batches each (see HS in the kernel); 1 = one head batch
+// of 32/LPR token rows, as every other mode.
+#ifndef H3QK_AMAX_HEAD_SPLIT
+#define H3QK_AMAX_HEAD_SPLIT 1
+#endif
+
 // 1: the amax pass walks each work item backwards (see kBack in the kernel).
 #ifndef H3QK_AMAX_BACK
 #define H3QK_AMAX_BACK 1
@@ -937,6 +944,19 @@ __device__ __forceinline__ int64_t item_of(const Params& p, int64_t r)
     return r / p.seq;
 }
 
+// Lane groups of a warp that share a token row (the amax head split, see HS
+// in the kernel), and the token rows of one work item.
+template <int MODE, int LPR>
+__host__ __device__ constexpr int head_split()
+{
+    return MODE == kAmax && (32 / LPR) % H3QK_AMAX_HEAD_SPLIT == 0 ? H3QK_AMAX_HEAD_SPLIT : 1;
+}
+template <int MODE, int LPR>
+__host__ __device__ constexpr int rows_per_item()
+{
+    return 32 / LPR / head_split<MODE, LPR>();
+}
+
 template <bool BF16, int LPR, int CH, int MODE, bool SLICED, int RM>
 __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     qkprep_kernel(const __grid_constant__ Params p)
@@ -949,6 +969,16 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     constexpr int PF = TuneL<MODE, LPR>::PF;  // L2 prefetch distance in batches
     const int lane = threadIdx.x & 31;
     const int sub = lane / LPR;
+    // Head split (amax): the warp's TPW lane groups take RPG token rows, HS
+    // groups per row; group sub takes row sub / HS and, in each batch of HS*U
+    // head rows, the U heads from (sub % HS)*U.  A batch then reads HS*U
+    // consecutive head rows of each of its token rows (longer pieces of DRAM
+    // at a time) with the same copies per lane.
+    constexpr int HS = head_split<MODE, LPR>();
+    constexpr int RPG = rows_per_item<MODE, LPR>();
+    constexpr int HU = HS * U;   // head rows per batch and token row
+    const int srow = sub / HS;
+    const int hph = (sub % HS) * U;
     const int c = lane % LPR;
     bool on[CH];
 #pragma unroll
@@ -964,7 +994,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
     // and the second chunk of the lanes where rot1 is set; or any pattern.
     static_assert(RM == kRotAny || kPairs, "rotation modes other than kRotAny: e4m3 pair instances only");
     const bool rot1 = CH == 2 && 8 * (c + LPR) + 8 <= p.rotary_dim;
-    const int64_t n_groups = (p.rows + TPW - 1) / TPW;
+    const int64_t n_groups = (p.rows + RPG - 1) / RPG;
     // Work items: a row group, or (SLICED, for calls too small to fill the
     // GPU) one of 2^hs_shift slices of hs_heads heads of a row group.
     const int hs_shift = SLICED ? p.hs_shift : 0;
@@ -1068,8 +1098,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
             fh_lo = static_cast<int>(fit & hs_mask) * p.hs_heads;
             fh_hi = min(H, fh_lo + p.hs_heads);
         }
-        fh0 = kBack ? fh_lo + (fh_hi - fh_lo - 1) / U * U : fh_lo;
-        const int64_t rr = group_of(fit) * TPW + sub;
+        fh0 = kBack ? fh_lo + (fh_hi - fh_lo - 1) / HU * HU : fh_lo;
+        const int64_t rr = group_of(fit) * RPG + srow;
         bool ok = false;
         if (rr < p.rows) {
             const int64_t bb = item_of(p, rr);
@@ -1092,15 +1122,15 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                 for (int u = 0; u < U; ++u)
 #pragma unroll
                     for (int q = 0; q < CH; ++q)
-                        if (fh0 + u < fh_hi && fact[q]) {
+                        if (fh0 + hph + u < fh_hi && fact[q]) {
                             const uint16_t* src_u =
-                                frow + p.in_part_off[fpart] + static_cast<int64_t>(fh0 + u) * D + 8 * q * LPR;
+                                frow + p.in_part_off[fpart] + static_cast<int64_t>(fh0 + hph + u) * D + 8 * q * LPR;
                             if (dbg_in(p, src_u - p.qkv)) cp_async16(st + (u * CH + q) * 32 + lane, src_u);
                         }
                 if constexpr (kBack) {
-                    fh0 -= U;
+                    fh0 -= HU;
                     if (fh0 < fh_lo) {
-                        fh0 = fh_lo + (fh_hi - fh_lo - 1) / U * U;
+                        fh0 = fh_lo + (fh_hi - fh_lo - 1) / HU * HU;
                         if (fpart == 2 && has_qk) {
                             fpart = p.qk_end - 1;
                         } else if (fpart < 2 && fpart > p.qk_first) {
@@ -1112,7 +1142,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                         }
                     }
                 } else {
-                    fh0 += U;
+                    fh0 += HU;
                     if (fh0 >= fh_hi) {
                         fh0 = fh_lo;
                         if (fpart < 2 && fpart + 1 < p.qk_end) {
@@ -1178,7 +1208,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
         const int64_t g = group_of(it);
         const int h_lo = SLICED ? static_cast<int>(it & hs_mask) * p.hs_heads : 0;
         const int h_hi = SLICED ? min(H, h_lo + p.hs_heads) : H;
-        const int64_t r = g * TPW + sub;
+        const int64_t r = g * RPG + srow;
         int64_t b = 0, s = 0;
         bool act_row = false;
         if (r < p.rows) {
@@ -1274,8 +1304,9 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
         // ---- V: passed through ----------------------------------------------
         auto v_part = [&]() {
             const uint16_t* src = rowp + p.in_part_off[2];
-            const int hv_first = kBack ? h_lo + (h_hi - h_lo - 1) / UV * UV : h_lo;  // first batch of heads
-            for (int h0 = hv_first; kBack ? h0 >= h_lo : h0 < h_hi; h0 += kBack ? -UV : UV) {
+            constexpr int HUV = HS * UV;
+            const int hv_first = kBack ? h_lo + (h_hi - h_lo - 1) / HUV * HUV : h_lo;  // first batch of heads
+            for (int h0 = hv_first; kBack ? h0 >= h_lo : h0 < h_hi; h0 += kBack ? -HUV : HUV) {
                 prefetch(p.in_part_off[2] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(UV) * D);
                 uint4 raw[UV][CH];
                 if constexpr (S > 0) {
@@ -1294,16 +1325,19 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
 #pragma unroll
                         for (int q = 0; q < CH; ++q) {
                             raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
-                            if (h0 + u < h_hi && act[q]) {
-                                const uint16_t* a = src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR;
+                            if (h0 + hph + u < h_hi && act[q]) {
+                                const uint16_t* a = src + static_cast<int64_t>(h0 + hph + u) * D + 8 * q * LPR;
                                 if (dbg_in(p, a - p.qkv)) raw[u][q] = load16(a);
                             }
                         }
                 }
 #pragma unroll
                 for (int u = 0; u < UV; ++u) {
-                    const int h = h0 + u;
-                    if (h >= h_hi) break;  // warp-uniform
+                    const int h = h0 + hph + u;
+                    if (h >= h_hi) {
+                        if constexpr (HS == 1) break;  // warp-uniform
+                        else continue;  // head split (amax): no warp-wide step follows for V
+                    }
 #pragma unroll
                     for (int q = 0; q < CH; ++q) {
                         if (!act[q]) continue;
@@ -1336,8 +1370,8 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
             const int part = kBack ? 1 - pi : pi;
             if (part < p.qk_first || part >= p.qk_end) continue;  // warp-uniform
             const uint16_t* src = rowp + p.in_part_off[part];
-            const int h_first = kBack ? h_lo + (h_hi - h_lo - 1) / U * U : h_lo;  // first batch of heads
-            for (int h0 = h_first; kBack ? h0 >= h_lo : h0 < h_hi; h0 += kBack ? -U : U) {
+            const int h_first = kBack ? h_lo + (h_hi - h_lo - 1) / HU * HU : h_lo;  // first batch of heads
+            for (int h0 = h_first; kBack ? h0 >= h_lo : h0 < h_hi; h0 += kBack ? -HU : HU) {
                 prefetch(p.in_part_off[part] + static_cast<int64_t>(h0) * D, static_cast<int64_t>(U) * D);
                 if constexpr (MODE == kAmax) {
                     // Once per part: re-reading every batch made the three amax
@@ -1371,16 +1405,25 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
 #pragma unroll
                         for (int q = 0; q < CH; ++q) {
                             raw[u][q] = make_uint4(0u, 0u, 0u, 0u);
-                            if (h0 + u < h_hi && act[q]) {
-                                const uint16_t* a = src + static_cast<int64_t>(h0 + u) * D + 8 * q * LPR;
+                            if (h0 + hph + u < h_hi && act[q]) {
+                                const uint16_t* a = src + static_cast<int64_t>(h0 + hph + u) * D + 8 * q * LPR;
                                 if (dbg_in(p, a - p.qkv)) raw[u][q] = load16(a);
                             }
                         }
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const int h = h0 + u;
-                    if (h >= h_hi) break;  // warp-uniform
+                    const int h = h0 + hph + u;
+                    if constexpr (HS == 1) {
+                        if (h >= h_hi) break;  // warp-uniform
+                    }
+                    // With a head split the lane groups of a warp take different
+                    // heads, so a head past the slice is masked instead (the
+                    // steps below are warp-wide).
+                    const bool hrow = act_row && h < h_hi;
+                    bool acth[CH];
+#pragma unroll
+                    for (int q = 0; q < CH; ++q) acth[q] = act[q] && h < h_hi;
                     uint4 rw[CH];
 #pragma unroll
                     for (int q = 0; q < CH; ++q) rw[q] = raw[u][q];
@@ -1390,20 +1433,20 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                         // one), the row cannot raise the amax.
                         float t = 0.0f;
                         const float bnd = qk_bound<BF16, LPR, CH>(rw, wmax[part], p.inv_d, p.eps, D, t);
-                        const uint32_t bb = act_row ? __float_as_uint(bnd) : 0u;
+                        const uint32_t bb = hrow ? __float_as_uint(bnd) : 0u;
                         const uint32_t known = run[part] > thr[part] ? run[part] : thr[part];
                         if (__reduce_max_sync(0xffffffffu, bb) <= known) continue;  // warp-uniform
                         if constexpr (TPW >= H3QK_AMAX_PAIR_MIN_TPW) {
                             // Where the first vote fails (a head with an outlier
                             // channel fails it in every row), the pairwise test
                             // lets most rows skip the exact path.
-                            bool may = act_row && !(bnd < 0x1p127f);
+                            bool may = hrow && !(bnd < 0x1p127f);
                             if constexpr (kPairs) {
-                                may = may || (act_row && qk_pair_may_exceed2<BF16, CH>(
+                                may = may || (hrow && qk_pair_may_exceed2<BF16, CH>(
                                                              rw, reinterpret_cast<const float2*>(&ws[part][c][0]),
                                                              t, __uint_as_float(known)));
                             } else {
-                                may = may || (act_row && qk_pair_may_exceed<BF16, CH>(
+                                may = may || (hrow && qk_pair_may_exceed<BF16, CH>(
                                                              rw, reinterpret_cast<const float4*>(&ws[part][c][0]),
                                                              t, __uint_as_float(known)));
                             }
@@ -1432,7 +1475,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                         pair_angles(cs2, sn2);
                         amf[part] = qk_row_pairs_amax<BF16, LPR, CH, RM>(
                             rw, reinterpret_cast<const float2*>(&ws[part][c][0]), cs2, sn2, rot, rot1, p.inv_d,
-                            p.eps, D, p.one2, p.mone2, act, amf[part]);
+                            p.eps, D, p.one2, p.mone2, acth, amf[part]);
                         run[part] = __reduce_max_sync(0xffffffffu, __float_as_uint(amf[part]));
                         if (run[part] > pub[part]) {  // warp-uniform
                             if (lane == 0 && dbg_slot(p, p.slot[part])) atomicMax(p.amax_words + p.slot[part], run[part]);
@@ -1460,7 +1503,7 @@ __global__ void __launch_bounds__(Shape<MODE, LPR>::NT, Shape<MODE, LPR>::MB)
                                           p.inv_d, p.eps, D, y);
 #pragma unroll
                     for (int q = 0; q < CH; ++q) {
-                        if (!act[q]) continue;
+                        if (!acth[q]) continue;
                         const int64_t off = obase + h * p.out_hstride + 8 * q * LPR;
                         if constexpr (MODE == kOut16) {
                             uint16_t* dst = static_cast<uint16_t*>(p.out[part]) + off;

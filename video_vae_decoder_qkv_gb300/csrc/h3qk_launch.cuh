@@ -76,7 +76,7 @@ cudaError_t launch_sliced(const h3qk::Params& p, cudaStream_t st)
             raised[dev] = true;
         }
     }
-    constexpr int64_t tpw = 32 / LPR;
+    constexpr int64_t tpw = h3qk::rows_per_item<MODE, LPR>();
     const int64_t groups = ((p.rows + tpw - 1) / tpw) << (SLICED ? p.hs_shift : 0);
     const int64_t want = (groups + W - 1) / W;
     int64_t cap = static_cast<int64_t>(h3qk_internal_sm_count()) * H3QK_BLOCKS_PER_SM;
@@ -143,7 +143,7 @@ cudaError_t launch_rm(const h3qk::Params& p, cudaStream_t st)
 template <bool BF16, int LPR, int CH, int MODE>
 cudaError_t launch_one(const h3qk::Params& p0, cudaStream_t st)
 {
-    constexpr int64_t tpw = 32 / LPR;
+    constexpr int64_t tpw = h3qk::rows_per_item<MODE, LPR>();
     const int64_t groups = (p0.rows + tpw - 1) / tpw;
     const int64_t target = static_cast<int64_t>(h3qk_internal_sm_count()) * 16;
     const int heads = p0.heads;
