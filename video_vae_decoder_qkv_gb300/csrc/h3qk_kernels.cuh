@@ -179,25 +179,11 @@ constexpr int small_code()
                           : (MODE == kAmax ? H3QK_SMALL_AMAX
                                            : (MODE == kCast || MODE == kCastCount ? H3QK_SMALL_CAST : H3QK_SMALL_SAGE));
 }
-// Block shape of the other amax and cast instances as the same "W MB" code;
-// 0 keeps kWarpsPerBlock warps and the MIN_BLOCKS digit of the tuning code.
-#ifndef H3QK_LARGE_AMAX
-#define H3QK_LARGE_AMAX 0
-#endif
-#ifndef H3QK_LARGE_CAST
-#define H3QK_LARGE_CAST 0
-#endif
-template <int MODE>
-constexpr int large_code()
-{
-    return MODE == kAmax ? H3QK_LARGE_AMAX : (MODE == kCast || MODE == kCastCount ? H3QK_LARGE_CAST : 0);
-}
 template <int MODE, int LPR>
 struct Shape {
     static constexpr bool kSmall = LPR <= 4;
-    static constexpr int kCode = kSmall ? small_code<MODE>() : large_code<MODE>();
-    static constexpr int W = kCode ? kCode / 10 : kWarpsPerBlock;  // warps per block
-    static constexpr int MB = kCode ? kCode % 10 : Tune<MODE>::MB;  // blocks per SM
+    static constexpr int W = kSmall ? small_code<MODE>() / 10 : kWarpsPerBlock;  // warps per block
+    static constexpr int MB = kSmall ? small_code<MODE>() % 10 : Tune<MODE>::MB;  // blocks per SM
     static constexpr int NT = 32 * W;                                          // threads per block
     static_assert(W >= 1 && W <= 32 && MB >= 1, "block shape code: warps 1..32, blocks per SM >= 1");
 };
