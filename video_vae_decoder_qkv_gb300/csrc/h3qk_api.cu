@@ -74,7 +74,9 @@ static __device__ __align__(16) unsigned int g_dbg_status[4];
 #endif
 namespace {
 std::mutex g_dbg_mu;
+#if H3QK_DEBUG_CHECKS
 unsigned int* g_dbg_addr[kMaxDevices] = {nullptr};
+#endif
 int64_t g_dbg_out_limit = -1;  // < 0: the call's own output extent
 }  // namespace
 
